@@ -1,1 +1,150 @@
-"""GB300-native Kimi-K3 attention-residual (AttnRes) mixture."""
+"""GB300-native Kimi-K3 attention-residual (AttnRes) mixture.
+
+Thin Python binding of the C ABI in ``include/attn_res.h``.  Every step of the
+mixture runs in the sm_103a kernels of ``libattn_res.so``; this module only
+turns torch tensors into pointers, strides and a stream.  There is no CPU or
+PyTorch fallback: if the library is not built, calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+from ._build import LIB as LIB_PATH
+
+HIDDEN = 7168
+MAX_BLOCKS = 8
+
+FLAG_PDL = 0x1
+
+
+def FLAG_SPLIT(k: int) -> int:
+    return (int(k) & 0xFF) << 8
+
+
+STATUS = {0: "ATTN_RES_OK", 1: "ATTN_RES_EINVAL", 2: "ATTN_RES_EALIGN",
+          3: "ATTN_RES_EALIAS", 4: "ATTN_RES_ECUDA", 5: "ATTN_RES_EDEVICE"}
+
+# Every symbol the header declares.
+EXPORTS = ("attn_res", "attn_res_status_string", "attn_res_hidden_size",
+           "attn_res_max_blocks", "attn_res_launch_shape")
+
+
+class Layout(ctypes.Structure):
+    """attn_res_layout_t"""
+    _fields_ = [("prefix_row", ctypes.c_int64), ("delta_row", ctypes.c_int64),
+                ("blocks_token", ctypes.c_int64), ("blocks_slot", ctypes.c_int64),
+                ("out_row", ctypes.c_int64), ("blocks_capacity", ctypes.c_int32),
+                ("flags", ctypes.c_uint32)]
+
+
+class AttnResError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS.get(status, status)}: {message}")
+        self.status = status
+
+
+_lib = None
+
+
+def library_path() -> str:
+    return LIB_PATH
+
+
+def lib():
+    """The loaded libattn_res.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"{LIB_PATH} is missing: build it with "
+                "attention_residual_fusion_gb300._build.build() (or __graft_entry__.build())")
+        L = ctypes.CDLL(LIB_PATH)
+        vp = ctypes.c_void_p
+        L.attn_res.restype = ctypes.c_int
+        L.attn_res.argtypes = [vp, vp, vp, ctypes.c_int, ctypes.c_int, vp, vp, vp,
+                               ctypes.c_float, ctypes.c_float, vp, ctypes.c_int64,
+                               ctypes.POINTER(Layout), vp]
+        L.attn_res_status_string.restype = ctypes.c_char_p
+        L.attn_res_status_string.argtypes = [ctypes.c_int]
+        L.attn_res_hidden_size.restype = ctypes.c_int
+        L.attn_res_hidden_size.argtypes = []
+        L.attn_res_max_blocks.restype = ctypes.c_int
+        L.attn_res_max_blocks.argtypes = []
+        L.attn_res_launch_shape.restype = ctypes.c_int
+        L.attn_res_launch_shape.argtypes = [
+            ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_uint32,
+            ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int),
+            ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int)]
+        _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().attn_res_status_string(status).decode()
+
+
+def launch_shape(T: int, num_blocks: int, has_out_norm: bool, flags: int = 0) -> dict:
+    """Launch attn_res would make: split, threads per CTA, CTAs, cluster size."""
+    k, th, cl = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+    ctas = ctypes.c_int64()
+    st = lib().attn_res_launch_shape(T, num_blocks, int(has_out_norm), flags,
+                                     ctypes.byref(k), ctypes.byref(th),
+                                     ctypes.byref(ctas), ctypes.byref(cl))
+    if st != 0:
+        raise AttnResError(st, status_string(st))
+    return dict(split=k.value, threads=th.value, ctas=ctas.value, cluster=cl.value)
+
+
+def call_raw(prefix: int, delta: int, blocks: int, num_blocks: int,
+             block_write_idx: int, res_w: int, rms_w: int, out_norm_w: int,
+             eps: float, out_eps: float, out: int, T: int, layout: Layout,
+             stream: int) -> int:
+    """The C entry point on raw addresses; returns the status code."""
+    return lib().attn_res(prefix or None, delta or None, blocks or None,
+                          num_blocks, block_write_idx, res_w or None,
+                          rms_w or None, out_norm_w or None, eps, out_eps,
+                          out or None, T, ctypes.byref(layout), stream or None)
+
+
+def _ptr(t) -> int:
+    return 0 if t is None else int(t.data_ptr())
+
+
+def attn_res(prefix, delta, blocks, num_blocks: int, block_write_idx: int,
+             res_w, rms_w, out_norm_w=None, eps: float = 1e-6,
+             out_eps: float = 1e-6, out=None, *, pdl: bool = False,
+             split: int = 0, stream=None):
+    """AttnRes mixture on CUDA bf16 tensors (see include/attn_res.h).
+
+    prefix [T, H] (updated in place when ``delta`` is given), delta [T, H] or
+    None, blocks [T, capacity, H] (any token/slot strides, unit inner stride;
+    slot ``block_write_idx`` is overwritten when >= 0), res_w / rms_w /
+    out_norm_w [H].  Returns ``out`` [T, H] (allocated if not given).
+    """
+    import torch
+
+    T = prefix.shape[0]
+    if out is None:
+        out = torch.empty((T, HIDDEN), dtype=prefix.dtype, device=prefix.device)
+    for name, t in (("prefix", prefix), ("delta", delta), ("out", out)):
+        if t is not None and (t.dim() != 2 or t.stride(1) != 1):
+            raise ValueError(f"{name} must be a [T, H] tensor with unit inner stride")
+    if blocks is not None and (blocks.dim() != 3 or blocks.stride(2) != 1):
+        raise ValueError("blocks must be a [T, capacity, H] tensor with unit inner stride")
+    lay = Layout(prefix_row=prefix.stride(0),
+                 delta_row=delta.stride(0) if delta is not None else 0,
+                 blocks_token=blocks.stride(0) if blocks is not None else 0,
+                 blocks_slot=blocks.stride(1) if blocks is not None else 0,
+                 out_row=out.stride(0),
+                 blocks_capacity=blocks.shape[1] if blocks is not None else 0,
+                 flags=(FLAG_PDL if pdl else 0) | FLAG_SPLIT(split))
+    if stream is None:
+        stream = torch.cuda.current_stream(prefix.device)
+    st = call_raw(_ptr(prefix), _ptr(delta), _ptr(blocks), num_blocks,
+                  block_write_idx, _ptr(res_w), _ptr(rms_w), _ptr(out_norm_w),
+                  eps, out_eps, _ptr(out), T, lay, int(stream.cuda_stream))
+    if st != 0:
+        raise AttnResError(st, status_string(st))
+    return out

@@ -1,0 +1,470 @@
+#!/usr/bin/env python
+"""Benchmark of the AttnRes mixture on GB300 (one JSON line on stdout).
+
+A step is one attn_res call over the whole workload (every step of the path
+runs in it).  Default workload: long prefill, T=8192 tokens, 8 valid blocks
+in a 9-slot bank with padded slot stride 7232, delta and output norm on,
+write-back into slot 8.  Its inputs (1.53 GB touched per step) are larger
+than L2, so no flush is needed between steps.
+
+  value      tokens/s, device time (CUDA events on the launching stream),
+             inputs resident in HBM, max over ranks, summed over ranks
+  e2e        the same metric through the public call with pinned HOST
+             buffers: every step copies its inputs host->device and reads
+             out, the updated prefix and the written bank slot back
+  roofline   algorithmic bytes per launch / mean launch time vs the measured
+             HBM copy bandwidth
+  latency_us T=1 latency (single-token and 8-block cases): per call with an
+             L2 flush in between, and back-to-back in a CUDA graph
+  cpu_baseline  the CPU oracle on a bounded sample of the same workload
+
+``--impl reference`` times the CPU oracle on the same workload and metric.
+Multi-GPU (torchrun): every rank runs its own copy of the workload on its own
+GPU (independent token rows, no collective on the data path: weak scaling).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = ("AttnRes µs/call at T=1 and tokens/s + achieved HBM GB/s "
+          "(% of peak) at T=1024–8192")
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ---- workloads ----------------------------------------------------------------
+
+def make(name: str):
+    from attention_residual_fusion_gb300 import workloads as W
+    if name == "long_prefill":
+        return W.long_prefill(), "long prefill T=8192, S=8, bank [8192,9,7232] padded, delta, output norm, write-back slot 8, per-block scales U(1,30)"
+    if name == "single_token":
+        return W.single_token(), "single token T=1, S=4, bank [1,8,7168], delta, output norm, no write-back"
+    kind, *a = name.split(":")
+    if kind == "prefill":          # prefill:T:S:o:w
+        T, S, o, w = (int(x) for x in a)
+        return W.prefill(T, S, bool(o), w), f"prefill T={T}, S={S}, delta, output norm {bool(o)}, write_idx {w}, 1% outliers x50"
+    if kind == "decode":           # decode:T
+        T = int(a[0])
+        return W.decode_batch(T), f"decode batch T={T}, S=8, delta, output norm, per-block scales U(0.5,20)"
+    if kind == "variant":          # variant:T:S:d:o:w
+        T, S, d, o, w = (int(x) for x in a)
+        return W.variant_cell(T, S, bool(d), bool(o), w), f"variant T={T}, S={S}, delta {bool(d)}, output norm {bool(o)}, write_idx {w}"
+    raise SystemExit(f"unknown workload {name}")
+
+
+def source_digest() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "attention_residual_fusion_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh")):
+            h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source and this workload."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    try:
+        d = json.load(open(p))
+    except Exception:
+        return None
+    e = d.get(workload)
+    if not e or e.get("source_digest") != source_digest():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+# ---- clocks -------------------------------------------------------------------
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.t.join(timeout=5)
+
+    def summary(self):
+        if self.proc is None:
+            return None
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---- CPU oracle -----------------------------------------------------------------
+
+def oracle_rate(wl, budget_s: float, threads: int):
+    """Tokens/s of the oracle on a bounded sample of the workload: the first
+    n token rows, repeated passes until about budget_s of CPU time."""
+    import oracle
+    n = min(wl.T, max(threads, 16))
+    t0 = time.perf_counter()
+    oracle.run_workload(wl, n_threads=threads, tokens=np.arange(n))
+    dt = time.perf_counter() - t0
+    n = int(min(wl.T, max(n, n * budget_s / max(dt, 1e-6))))
+    toks = np.arange(n)
+    passes, t0 = 0, time.perf_counter()
+    while True:
+        oracle.run_workload(wl, n_threads=threads, tokens=toks)
+        passes += 1
+        dt = time.perf_counter() - t0
+        if dt >= budget_s or passes >= 1000:
+            break
+    return n * passes / dt, n, passes, dt
+
+
+# ---- GPU arm ------------------------------------------------------------------
+
+def device_tensors(wl, torch, dev):
+    def up(a):
+        return torch.from_numpy(a.view(np.int16)).to(dev).view(torch.bfloat16)
+    return dict(prefix=up(wl.prefix), delta=None if wl.delta is None else up(wl.delta),
+                bank=up(wl.bank), rms=up(wl.rms_w), res=up(wl.res_w),
+                onw=None if wl.out_norm_w is None else up(wl.out_norm_w),
+                out=torch.empty((wl.T, wl.H), dtype=torch.bfloat16, device=dev))
+
+
+def call(ar, wl, t, stream, split=0, pdl=False):
+    ar.attn_res(t["prefix"], t["delta"], t["bank"][:, :, : wl.H], wl.num_blocks,
+                wl.block_write_idx, t["res"], t["rms"], t["onw"], wl.eps, wl.out_eps,
+                t["out"], split=split, pdl=pdl, stream=stream)
+
+
+def time_device(ar, wl, t, torch, stream, steps, warmup, split=0):
+    for _ in range(warmup):
+        call(ar, wl, t, stream, split)
+    torch.cuda.synchronize()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    with torch.cuda.stream(stream):
+        ev[0].record(stream)
+        for i in range(steps):
+            call(ar, wl, t, stream, split)
+            ev[i + 1].record(stream)
+    torch.cuda.synchronize()
+    per = [ev[i].elapsed_time(ev[i + 1]) for i in range(steps)]
+    return ev[0].elapsed_time(ev[steps]), per
+
+
+def latency_t1(ar, torch, dev, stream, reps=200):
+    """T=1 latency: per call with L2 flushed between calls (events around each
+    call), and back-to-back inside a captured CUDA graph."""
+    from attention_residual_fusion_gb300 import workloads as W
+    res = {}
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    for name, wl in (("single_token_T1_S4", W.single_token()),
+                     ("T1_S8_delta_norm", W.variant_cell(1, 8, True, True, -1))):
+        t = device_tensors(wl, torch, dev)
+        for _ in range(10):
+            call(ar, wl, t, stream)
+        times = []
+        for _ in range(reps):
+            with torch.cuda.stream(stream):
+                flush.fill_(1.0)
+                a = torch.cuda.Event(enable_timing=True)
+                b = torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                call(ar, wl, t, stream)
+                b.record(stream)
+            b.synchronize()
+            times.append(a.elapsed_time(b) * 1e3)
+        g = torch.cuda.CUDAGraph()
+        n = 100
+        with torch.cuda.graph(g, stream=stream):
+            for _ in range(n):
+                call(ar, wl, t, stream)
+        g.replay()
+        torch.cuda.synchronize()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            a.record(stream)
+            for _ in range(5):
+                g.replay()
+            b.record(stream)
+        torch.cuda.synchronize()
+        res[name] = {"flushed_p50": round(statistics.median(times), 3),
+                     "flushed_p20": round(float(np.percentile(times, 20)), 3),
+                     "flushed_p80": round(float(np.percentile(times, 80)), 3),
+                     "graph_per_call": round(a.elapsed_time(b) * 1e3 / (5 * n), 3)}
+        del t, g
+    del flush
+    return res
+
+
+def e2e(ar, wl, torch, dev, stream, steps):
+    """Through the public call with pinned host buffers: H2D of every input,
+    the call, D2H of out, the updated prefix and the written bank slot."""
+    pin = lambda a: torch.from_numpy(a.view(np.int16)).pin_memory().view(torch.bfloat16)
+    hp = dict(prefix=pin(wl.prefix), delta=None if wl.delta is None else pin(wl.delta),
+              bank=pin(wl.bank), rms=pin(wl.rms_w), res=pin(wl.res_w),
+              onw=None if wl.out_norm_w is None else pin(wl.out_norm_w))
+    d = device_tensors(wl, torch, dev)
+    h_out = torch.empty((wl.T, wl.H), dtype=torch.bfloat16).pin_memory()
+    h_pre = torch.empty((wl.T, wl.H), dtype=torch.bfloat16).pin_memory()
+    h_slot = torch.empty((wl.T, wl.H), dtype=torch.bfloat16).pin_memory() \
+        if wl.block_write_idx >= 0 else None
+    h2d = sum(v.numel() * 2 for v in hp.values() if v is not None)
+    d2h = h_out.numel() * 2 + (h_pre.numel() * 2 if wl.delta is not None else 0) + \
+        (h_slot.numel() * 2 if h_slot is not None else 0)
+
+    def step():
+        with torch.cuda.stream(stream):
+            for k, v in hp.items():
+                if v is not None:
+                    d[k].copy_(v, non_blocking=True)
+            call(ar, wl, d, stream)
+            h_out.copy_(d["out"], non_blocking=True)
+            if wl.delta is not None:
+                h_pre.copy_(d["prefix"], non_blocking=True)
+            if h_slot is not None:
+                h_slot.copy_(d["bank"][:, wl.block_write_idx, : wl.H], non_blocking=True)
+
+    step()
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        a.record(stream)
+    w0 = time.perf_counter()
+    for _ in range(steps):
+        step()
+    with torch.cuda.stream(stream):
+        b.record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - w0
+    ms = a.elapsed_time(b)
+    del d, hp
+    return {"value": wl.T * steps / (ms / 1e3), "unit": "tokens/s",
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "steps": steps, "ms_per_step": ms / steps,
+            "host_wall_ms_per_step": wall * 1e3 / steps}
+
+
+def run_ours(args, rank, world, local_rank, dist):
+    import torch
+    import attention_residual_fusion_gb300 as ar
+    from attention_residual_fusion_gb300 import _build
+
+    _build.build()
+    ar.lib()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    wl, desc = make(args.workload)
+    t = device_tensors(wl, torch, dev)
+    stream = torch.cuda.Stream(dev)
+    shape = ar.launch_shape(wl.T, wl.num_blocks, wl.out_norm_w is not None,
+                            ar.FLAG_SPLIT(args.split))
+
+    for _ in range(max(args.warmup, 3)):
+        call(ar, wl, t, stream, args.split)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local_rank) as clk:
+        total_ms, per = time_device(ar, wl, t, torch, stream, args.steps, 0, args.split)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    tmax = total_ms
+    if dist is not None:
+        x = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(x, op=dist.ReduceOp.MAX)
+        tmax = float(x.item())
+    tokens_total = wl.T * args.steps * world
+    value = tokens_total / (tmax / 1e3)
+    mean_launch_ms = statistics.mean(per)
+    alg_bytes = wl.algorithmic_bytes()
+    peak, peak_kind = measured_peaks()
+    achieved = alg_bytes / (mean_launch_ms / 1e3) / 1e9
+
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": max(args.warmup, 3),
+        "ms_per_step": round(tmax / args.steps, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "io_dtype": "bf16",
+        "data": "synthetic (seeded numpy, distributions of the pages' workloads)",
+        "config": {"workload": desc, "T": wl.T, "num_blocks": wl.num_blocks,
+                   "capacity": wl.capacity, "slot_stride": wl.slot_stride,
+                   "delta": wl.delta is not None, "output_norm": wl.out_norm_w is not None,
+                   "block_write_idx": wl.block_write_idx, "H": wl.H,
+                   "launch": shape, "pdl": False,
+                   "l2": f"inputs larger than L2 ({alg_bytes / 1e9:.2f} GB touched per step); no flush",
+                   "parallelism": f"replicas x{world} (token rows independent, no collective)"},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs, copy)",
+                     "algorithmic_bytes_per_launch": alg_bytes,
+                     "mean_launch_us": round(mean_launch_ms * 1e3, 3),
+                     "traffic": recorded_traffic(args.workload),
+                     "kernel": "attn_res_split_kernel"},
+        "gpu_launches": args.steps,
+        "clocks": clk.summary(),
+    }
+    if rank == 0 and not args.no_latency:
+        line["latency_us"] = latency_t1(ar, torch, dev, stream)
+    if not args.no_e2e:
+        del t
+        torch.cuda.empty_cache()
+        e = e2e(ar, wl, torch, dev, stream, max(3, min(args.steps, args.e2e_steps)))
+        if dist is not None:
+            x = torch.tensor([e["ms_per_step"]], dtype=torch.float64, device=dev)
+            dist.all_reduce(x, op=dist.ReduceOp.MAX)
+            e["ms_per_step"] = float(x.item())
+            e["value"] = wl.T * world / (e["ms_per_step"] / 1e3)
+        e["value"] = round(e["value"], 1)
+        line["e2e"] = e
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        threads = os.cpu_count() or 1
+        rate, n, passes, dt = oracle_rate(wl, args.cpu_budget, threads)
+        line["cpu_baseline"] = {"value": round(rate, 2), "unit": "tokens/s", "cores": threads,
+                                "kind": "oracle",
+                                "sample": f"first {n} token rows of the same workload, {passes} pass(es), {dt:.1f} s"}
+    return line
+
+
+def run_reference(args, rank, world):
+    """The CPU oracle as the reference arm, on rank 0 only."""
+    if rank != 0:
+        return None
+    import oracle
+    wl, desc = make(args.workload)
+    threads = os.cpu_count() or 1
+    # one step = a bounded sample of the workload, sized so that the whole run
+    # stays within a few minutes
+    n = min(wl.T, max(threads, 16))
+    t0 = time.perf_counter()
+    oracle.run_workload(wl, n_threads=threads, tokens=np.arange(n))
+    per_tok = (time.perf_counter() - t0) / n
+    steps_total = args.steps + args.warmup
+    n = int(min(wl.T, max(threads, args.ref_budget / max(steps_total, 1) / per_tok)))
+    toks = np.arange(n)
+    for _ in range(args.warmup):
+        oracle.run_workload(wl, n_threads=threads, tokens=toks)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.run_workload(wl, n_threads=threads, tokens=toks)
+    dt = time.perf_counter() - t0
+    value = n * args.steps / dt
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 2), "unit": "tokens/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(dt * 1e3 / args.steps, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "io_dtype": "bf16",
+            "data": "synthetic (seeded numpy)",
+            "config": {"workload": desc, "T": wl.T, "sample_tokens_per_step": n},
+            "cpu_baseline": {"value": round(value, 2), "unit": "tokens/s", "cores": threads,
+                             "kind": "oracle",
+                             "sample": f"first {n} token rows of the workload per step"},
+            "e2e": {"value": round(value, 2), "unit": "tokens/s",
+                    "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="long_prefill")
+    ap.add_argument("--split", type=int, default=0, help="CTAs per token row (0 = automatic)")
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--cpu-budget", type=float, default=10.0)
+    ap.add_argument("--ref-budget", type=float, default=60.0)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-latency", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as tdist
+        torch.cuda.set_device(local_rank)
+        tdist.init_process_group("nccl")
+        dist = tdist
+    line = run_ours(args, rank, world, local_rank, dist)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

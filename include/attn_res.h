@@ -1,0 +1,154 @@
+/*
+ * attn_res.h -- C ABI of the GB300-native Kimi-K3 attention-residual
+ * (AttnRes) mixture.
+ *
+ * The operation (implementation walkthrough of vllm-ascend PR #14840 "Add
+ * Kimi K3 attention residual fusion"; key source excerpts of the prhub summary
+ * of vllm PR #54261 "SM100 Kimi-K3 AttnRes defaults to native CUDA"): for each
+ * token row t of width H = 7168,
+ *
+ *   c      = bf16_rn(prefix[t] + delta[t])      (c = prefix[t] if no delta)
+ *   x_i    = blocks[t, i]  for i < num_blocks,  x_S = c        (S = num_blocks)
+ *   q      = rms_w * res_w
+ *   l_i    = <x_i, q> / sqrt(mean(x_i^2) + eps)
+ *   w      = softmax(l_0 .. l_S)
+ *   acc    = sum_i w_i x_i                      (raw rows, fp32)
+ *   out[t] = bf16_rn(acc * out_norm_w / sqrt(mean(acc^2) + out_eps))
+ *            or bf16_rn(acc) when out_norm_w == NULL
+ *   prefix[t] = c                  when delta != NULL          (in place)
+ *   blocks[t, block_write_idx] = c when block_write_idx >= 0   (in place)
+ *
+ * All reads of a token see the values from before the call, so a write-back
+ * slot may also be one of the sources (block_write_idx < num_blocks).
+ *
+ * Element type: every tensor is bf16, passed as a pointer to its 16-bit
+ * patterns (uint16_t).  Strides are in elements.  All tensor pointers are
+ * DEVICE pointers of the current CUDA device; the caller owns every buffer.
+ * The library allocates no memory, keeps no per-call state and is
+ * re-entrant.
+ */
+#ifndef ATTN_RES_H_
+#define ATTN_RES_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Hidden size the kernels are built for (the Kimi-K3 width named in the
+ * dispatch gate of vllm PR #54261). */
+#define ATTN_RES_HIDDEN 7168
+/* Largest num_blocks (same gate: 0 <= num_blocks <= 8). */
+#define ATTN_RES_MAX_BLOCKS 8
+
+typedef uint16_t attn_res_bf16_t; /* bf16 bit pattern */
+
+typedef enum {
+  ATTN_RES_OK = 0,
+  ATTN_RES_EINVAL = 1,  /* a size, index, stride, eps or required pointer is invalid */
+  ATTN_RES_EALIGN = 2,  /* a pointer is not 16-byte aligned or a stride is not a multiple of 8 */
+  ATTN_RES_EALIAS = 3,  /* a written region overlaps another argument's region */
+  ATTN_RES_ECUDA = 4,   /* the CUDA runtime reported an error (query, attribute or launch) */
+  ATTN_RES_EDEVICE = 5  /* the current device is not a compute capability 10.3 GPU */
+} attn_res_status_t;
+
+/* Launch options, in attn_res_layout_t.flags. */
+
+/* Programmatic dependent launch: the kernel may start while the previous
+ * kernel of the stream is still running.  It loads the bank rows and the
+ * weights first, then waits for that kernel (griddepcontrol.wait) before
+ * reading prefix and delta, and lets its own dependents launch once those
+ * loads are issued.  Contract: the bank rows read and the weights must not be
+ * written by the immediately preceding kernel of the stream.  Placement of
+ * the wait: PDL discipline in the key source excerpts of vllm PR #54261. */
+#define ATTN_RES_FLAG_PDL 0x1u
+
+/* Tuning override: the number of CTAs (one thread-block cluster) a token row
+ * is split over.  0 = automatic.  Accepted: 4, 7, 8, 14, 16.  Results do not
+ * depend on it beyond fp32 summation order. */
+#define ATTN_RES_FLAG_SPLIT(k) (((uint32_t)(k) & 0xffu) << 8)
+
+/* Memory layout of the tensors, in elements.  A row is H contiguous
+ * elements; columns H .. stride-1 are padding that is never read or
+ * written. */
+typedef struct {
+  int64_t prefix_row;      /* between token rows of prefix (>= H) */
+  int64_t delta_row;       /* between token rows of delta (>= H; ignored if delta == NULL) */
+  int64_t blocks_token;    /* between tokens of the bank (>= (capacity-1)*blocks_slot + H when T > 1) */
+  int64_t blocks_slot;     /* between slots of one token (>= H) */
+  int64_t out_row;         /* between token rows of out (>= H) */
+  int32_t blocks_capacity; /* slots allocated per token (blocks.shape[1]); >= num_blocks */
+  uint32_t flags;          /* ATTN_RES_FLAG_* */
+} attn_res_layout_t;
+
+/*
+ * attn_res -- enqueue the AttnRes mixture for T token rows on `stream`.
+ *
+ *   prefix          [T, H] at prefix_row.  Read; overwritten with c when
+ *                   delta != NULL.
+ *   delta           [T, H] at delta_row, or NULL.
+ *   blocks          bank [T, capacity, H] at (blocks_token, blocks_slot).
+ *                   Slots 0 .. num_blocks-1 are read; slot block_write_idx
+ *                   (if >= 0) is overwritten with c; nothing else is touched.
+ *                   May be NULL only when num_blocks == 0 and
+ *                   block_write_idx == -1.
+ *   num_blocks      valid bank slots S, 0 <= S <= min(8, capacity).
+ *   block_write_idx -1 (no write-back) or 0 <= idx < capacity.
+ *   res_w, rms_w    [H] weights (the reference's proj / qk weight and norm
+ *                   weight); q = rms_w * res_w.
+ *   out_norm_w      [H] output RMSNorm weight, or NULL for no output norm.
+ *   eps, out_eps    finite, >= 0.
+ *   out             [T, H] at out_row.
+ *   T               token rows, >= 0.  T == 0 checks the scalar arguments
+ *                   and returns OK; pointers and strides are not examined.
+ *   layout          strides, capacity and flags (see above).  Not NULL.
+ *   stream          a cudaStream_t of the current device (NULL = legacy
+ *                   default stream).
+ *
+ * Requirements: all pointers 16-byte aligned; all strides multiples of 8;
+ * the address range [ptr, ptr + extent) of each written tensor (out always,
+ * prefix when delta != NULL, blocks when block_write_idx >= 0) does not
+ * overlap the range of any other argument.
+ *
+ * Returns ATTN_RES_OK once the work is enqueued (the call is asynchronous).
+ * Any other status is returned before anything is launched, and nothing is
+ * written.  Faults during execution surface from later CUDA calls on the
+ * stream, as for any kernel.
+ */
+attn_res_status_t attn_res(attn_res_bf16_t* prefix, const attn_res_bf16_t* delta,
+                           attn_res_bf16_t* blocks, int num_blocks,
+                           int block_write_idx, const attn_res_bf16_t* res_w,
+                           const attn_res_bf16_t* rms_w,
+                           const attn_res_bf16_t* out_norm_w, float eps,
+                           float out_eps, attn_res_bf16_t* out, int64_t T,
+                           const attn_res_layout_t* layout, void* stream);
+
+/* Static text for a status code. */
+const char* attn_res_status_string(attn_res_status_t status);
+
+/* ATTN_RES_HIDDEN, for callers that load the library dynamically. */
+int attn_res_hidden_size(void);
+
+/* ATTN_RES_MAX_BLOCKS. */
+int attn_res_max_blocks(void);
+
+/*
+ * attn_res_launch_shape -- the launch attn_res would make for T rows with
+ * num_blocks sources, output norm on/off and the given flags: CTAs per token
+ * row (`split`, 1 when the CTAs need not talk to each other), threads per
+ * CTA, CTAs in the grid and the thread-block cluster size (1 = no cluster).
+ * Pure host computation, no CUDA call.  Returns ATTN_RES_EINVAL for T < 0,
+ * num_blocks outside 0..8 or an unsupported split override.
+ */
+attn_res_status_t attn_res_launch_shape(int64_t T, int num_blocks,
+                                        int has_out_norm, uint32_t flags,
+                                        int* split, int* threads_per_cta,
+                                        int64_t* ctas, int* cluster);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_RES_H_ */
