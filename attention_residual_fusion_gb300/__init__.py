@@ -17,10 +17,24 @@ HIDDEN = 7168
 MAX_BLOCKS = 8
 
 FLAG_PDL = 0x1
+KERNEL_SPLIT = 1
+KERNEL_STREAM = 2
 
 
 def FLAG_SPLIT(k: int) -> int:
     return (int(k) & 0xFF) << 8
+
+
+def FLAG_KERNEL(k: int) -> int:
+    return (int(k) & 0xF) << 16
+
+
+def FLAG_STAGES(n: int) -> int:
+    return (int(n) & 0xF) << 20
+
+
+def FLAG_VPT(n: int) -> int:
+    return (int(n) & 0xF) << 24
 
 
 STATUS = {0: "ATTN_RES_OK", 1: "ATTN_RES_EINVAL", 2: "ATTN_RES_EALIGN",
@@ -28,7 +42,7 @@ STATUS = {0: "ATTN_RES_OK", 1: "ATTN_RES_EINVAL", 2: "ATTN_RES_EALIGN",
 
 # Every symbol the header declares.
 EXPORTS = ("attn_res", "attn_res_status_string", "attn_res_hidden_size",
-           "attn_res_max_blocks", "attn_res_launch_shape")
+           "attn_res_max_blocks", "attn_res_launch_shape", "attn_res_device_status")
 
 
 class Layout(ctypes.Structure):
@@ -73,10 +87,12 @@ def lib():
         L.attn_res_max_blocks.restype = ctypes.c_int
         L.attn_res_max_blocks.argtypes = []
         L.attn_res_launch_shape.restype = ctypes.c_int
+        ip = ctypes.POINTER(ctypes.c_int)
         L.attn_res_launch_shape.argtypes = [
             ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_uint32,
-            ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int),
-            ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int)]
+            ip, ip, ip, ip, ctypes.POINTER(ctypes.c_int64), ip]
+        L.attn_res_device_status.restype = ctypes.c_int
+        L.attn_res_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint), ctypes.c_int]
         _lib = L
     return _lib
 
@@ -86,15 +102,27 @@ def status_string(status: int) -> str:
 
 
 def launch_shape(T: int, num_blocks: int, has_out_norm: bool, flags: int = 0) -> dict:
-    """Launch attn_res would make: split, threads per CTA, CTAs, cluster size."""
-    k, th, cl = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+    """Launch attn_res would make: kernel, split, stages, threads per CTA,
+    CTAs (0 = persistent grid sized to the device) and cluster size."""
+    kern, k, st_, th, cl = (ctypes.c_int() for _ in range(5))
     ctas = ctypes.c_int64()
     st = lib().attn_res_launch_shape(T, num_blocks, int(has_out_norm), flags,
-                                     ctypes.byref(k), ctypes.byref(th),
+                                     ctypes.byref(kern), ctypes.byref(k),
+                                     ctypes.byref(st_), ctypes.byref(th),
                                      ctypes.byref(ctas), ctypes.byref(cl))
     if st != 0:
         raise AttnResError(st, status_string(st))
-    return dict(split=k.value, threads=th.value, ctas=ctas.value, cluster=cl.value)
+    return dict(kernel={1: "split", 2: "stream"}[kern.value], split=k.value,
+                stages=st_.value, threads=th.value, ctas=ctas.value, cluster=cl.value)
+
+
+def device_status(clear: bool = False) -> int:
+    """Error bits recorded by the kernels on the current device (0 = none)."""
+    bits = ctypes.c_uint()
+    st = lib().attn_res_device_status(ctypes.byref(bits), int(clear))
+    if st != 0:
+        raise AttnResError(st, status_string(st))
+    return bits.value
 
 
 def call_raw(prefix: int, delta: int, blocks: int, num_blocks: int,
@@ -115,7 +143,8 @@ def _ptr(t) -> int:
 def attn_res(prefix, delta, blocks, num_blocks: int, block_write_idx: int,
              res_w, rms_w, out_norm_w=None, eps: float = 1e-6,
              out_eps: float = 1e-6, out=None, *, pdl: bool = False,
-             split: int = 0, stream=None):
+             split: int = 0, kernel: int = 0, stages: int = 0, vpt: int = 0,
+             stream=None):
     """AttnRes mixture on CUDA bf16 tensors (see include/attn_res.h).
 
     prefix [T, H] (updated in place when ``delta`` is given), delta [T, H] or
@@ -125,6 +154,11 @@ def attn_res(prefix, delta, blocks, num_blocks: int, block_write_idx: int,
     """
     import torch
 
+    for name, t in (("prefix", prefix), ("delta", delta), ("blocks", blocks),
+                    ("res_w", res_w), ("rms_w", rms_w), ("out_norm_w", out_norm_w),
+                    ("out", out)):
+        if t is not None and (t.dtype != torch.bfloat16 or t.device.type != "cuda"):
+            raise ValueError(f"{name} must be a CUDA bfloat16 tensor")
     T = prefix.shape[0]
     if out is None:
         out = torch.empty((T, HIDDEN), dtype=prefix.dtype, device=prefix.device)
@@ -139,7 +173,8 @@ def attn_res(prefix, delta, blocks, num_blocks: int, block_write_idx: int,
                  blocks_slot=blocks.stride(1) if blocks is not None else 0,
                  out_row=out.stride(0),
                  blocks_capacity=blocks.shape[1] if blocks is not None else 0,
-                 flags=(FLAG_PDL if pdl else 0) | FLAG_SPLIT(split))
+                 flags=(FLAG_PDL if pdl else 0) | FLAG_SPLIT(split) |
+                 FLAG_KERNEL(kernel) | FLAG_STAGES(stages) | FLAG_VPT(vpt))
     if stream is None:
         stream = torch.cuda.current_stream(prefix.device)
     st = call_raw(_ptr(prefix), _ptr(delta), _ptr(blocks), num_blocks,

@@ -21,22 +21,54 @@ using namespace attn_res_host;
 
 constexpr int64_t kMaxStride = int64_t(1) << 40;
 
-// Split of a token row over CTAs.  Few tokens: many small CTAs per token, so
-// one token's latency chain (load, reduce, exchange) runs on many SMs.  Many
-// tokens: 7 CTAs of 128 threads, all threads active.
-int auto_split(int64_t T) { return T <= 32 ? 8 : 7; }
+constexpr uint32_t kKnownFlags = ATTN_RES_FLAG_PDL | ATTN_RES_FLAG_SPLIT(0xff) |
+                                 ATTN_RES_FLAG_KERNEL(0xf) | ATTN_RES_FLAG_STAGES(0xf) |
+                                 ATTN_RES_FLAG_VPT(0xf);
 
-attn_res_status_t resolve_split(int64_t T, uint32_t flags, int* k_out) {
-  int k = static_cast<int>((flags >> 8) & 0xffu);
-  if (k == 0) k = auto_split(T);
-  if (split_index(k) < 0) return ATTN_RES_EINVAL;
-  *k_out = k;
+// From this many tokens on, the persistent stream kernel is used.
+constexpr int64_t kStreamMinTokens = 128;
+
+struct Plan {
+  int kernel;  // ATTN_RES_KERNEL_SPLIT or ATTN_RES_KERNEL_STREAM
+  int split;   // CTAs per token row
+  int stages;  // ring depth (stream kernel), 0 otherwise
+  int vpt;     // 16-byte vectors per thread and row
+  int shape;   // index into the stream kernel's shape table
+};
+
+// Few tokens: one cluster per token, many small CTAs per token, so one
+// token's latency chain (load, reduce, exchange) runs on many SMs at once.
+// Many tokens: persistent clusters of 4 CTAs, 2 vectors per thread (112
+// threads per CTA) and a 2-deep TMA ring -- the fastest stream shape on
+// GB300 at 1024..8192 tokens.
+attn_res_status_t make_plan(int64_t T, uint32_t flags, Plan* out) {
+  Plan pl;
+  pl.kernel = static_cast<int>((flags >> 16) & 0xfu);
+  pl.split = static_cast<int>((flags >> 8) & 0xffu);
+  pl.stages = static_cast<int>((flags >> 20) & 0xfu);
+  pl.vpt = static_cast<int>((flags >> 24) & 0xfu);
+  pl.shape = -1;
+  if (pl.kernel == 0) pl.kernel = T >= kStreamMinTokens ? ATTN_RES_KERNEL_STREAM : ATTN_RES_KERNEL_SPLIT;
+  if (pl.kernel == ATTN_RES_KERNEL_SPLIT) {
+    if (pl.split == 0) pl.split = T <= 32 ? 8 : 7;
+    if (pl.vpt == 0) pl.vpt = 1;
+    if (split_index(pl.split) < 0 || pl.stages != 0 || pl.vpt != 1) return ATTN_RES_EINVAL;
+  } else if (pl.kernel == ATTN_RES_KERNEL_STREAM) {
+    if (pl.split == 0) pl.split = 4;
+    if (pl.stages == 0) pl.stages = 2;
+    if (pl.vpt == 0) pl.vpt = 2;
+    pl.shape = stream_shape_index(pl.split, pl.vpt, pl.stages);
+    if (pl.shape < 0) return ATTN_RES_EINVAL;
+  } else {
+    return ATTN_RES_EINVAL;
+  }
+  *out = pl;
   return ATTN_RES_OK;
 }
 
-int threads_for_split(int k) {
+int threads_for(int k, int vpt) {
   const int vpc = attn_res_dev::kNV / k;
-  return (vpc + 31) / 32 * 32;
+  return (vpc / vpt + 31) / 32 * 32;
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -64,6 +96,24 @@ bool overlaps(const Region& a, const Region& b) {
 // Per-device result of the compute-capability check: 0 unknown, 1 ok, 2 not ok.
 std::atomic<int> g_device_state[64];
 
+// Device status word: error bits a kernel records instead of hanging (a
+// stage wait that timed out).  One per device, for the life of the process.
+__device__ unsigned int g_status_word;
+std::atomic<uintptr_t> g_status_addr[64];
+
+cudaError_t status_word(int dev, unsigned** out) {
+  uintptr_t a = g_status_addr[dev].load(std::memory_order_acquire);
+  if (a == 0) {
+    void* ptr = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&ptr, g_status_word);
+    if (e != cudaSuccess) return e;
+    a = reinterpret_cast<uintptr_t>(ptr);
+    g_status_addr[dev].store(a, std::memory_order_release);
+  }
+  *out = reinterpret_cast<unsigned*>(a);
+  return cudaSuccess;
+}
+
 attn_res_status_t check_device(int* dev_out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -88,6 +138,21 @@ attn_res_status_t check_device(int* dev_out) {
     g_device_state[dev].store(st, std::memory_order_release);
   }
   return st == 1 ? ATTN_RES_OK : ATTN_RES_EDEVICE;
+}
+
+StreamLaunchFn lookup_stream(int S, int shape, bool d, bool o) {
+  switch (S) {
+    case 0: return stream_launcher_s0(shape, d, o);
+    case 1: return stream_launcher_s1(shape, d, o);
+    case 2: return stream_launcher_s2(shape, d, o);
+    case 3: return stream_launcher_s3(shape, d, o);
+    case 4: return stream_launcher_s4(shape, d, o);
+    case 5: return stream_launcher_s5(shape, d, o);
+    case 6: return stream_launcher_s6(shape, d, o);
+    case 7: return stream_launcher_s7(shape, d, o);
+    case 8: return stream_launcher_s8(shape, d, o);
+    default: return nullptr;
+  }
 }
 
 LaunchFn lookup(int S, int split_idx, bool d, bool o) {
@@ -126,17 +191,39 @@ int attn_res_max_blocks(void) { return ATTN_RES_MAX_BLOCKS; }
 
 attn_res_status_t attn_res_launch_shape(int64_t T, int num_blocks,
                                         int has_out_norm, uint32_t flags,
-                                        int* split, int* threads_per_cta,
-                                        int64_t* ctas, int* cluster) {
+                                        int* kernel, int* split, int* stages,
+                                        int* threads_per_cta, int64_t* ctas,
+                                        int* cluster) {
   if (T < 0 || num_blocks < 0 || num_blocks > ATTN_RES_MAX_BLOCKS) return ATTN_RES_EINVAL;
-  int k = 0;
-  attn_res_status_t st = resolve_split(T, flags, &k);
+  if ((flags & ~kKnownFlags) != 0) return ATTN_RES_EINVAL;
+  Plan pl;
+  attn_res_status_t st = make_plan(T, flags, &pl);
   if (st != ATTN_RES_OK) return st;
   const bool comm = num_blocks > 0 || has_out_norm;
-  if (split) *split = k;
-  if (threads_per_cta) *threads_per_cta = threads_for_split(k);
-  if (ctas) *ctas = T * k;
-  if (cluster) *cluster = comm ? k : 1;
+  if (kernel) *kernel = pl.kernel;
+  if (split) *split = pl.split;
+  if (stages) *stages = pl.stages;
+  if (threads_per_cta) *threads_per_cta = threads_for(pl.split, pl.vpt);
+  if (ctas) *ctas = pl.kernel == ATTN_RES_KERNEL_SPLIT ? T * pl.split : 0;
+  if (cluster) *cluster = comm ? pl.split : 1;
+  return ATTN_RES_OK;
+}
+
+attn_res_status_t attn_res_device_status(unsigned int* bits, int clear) {
+  if (bits == nullptr) return ATTN_RES_EINVAL;
+  int dev = 0;
+  attn_res_status_t st = check_device(&dev);
+  if (st != ATTN_RES_OK) return st;
+  unsigned* w = nullptr;
+  if (status_word(dev, &w) != cudaSuccess ||
+      cudaMemcpy(bits, w, sizeof(unsigned), cudaMemcpyDeviceToHost) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return ATTN_RES_ECUDA;
+  }
+  if (clear && cudaMemset(w, 0, sizeof(unsigned)) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return ATTN_RES_ECUDA;
+  }
   return ATTN_RES_OK;
 }
 
@@ -155,10 +242,10 @@ attn_res_status_t attn_res(attn_res_bf16_t* prefix, const attn_res_bf16_t* delta
   if (block_write_idx < -1 || block_write_idx >= cap) return ATTN_RES_EINVAL;
   if (!std::isfinite(eps) || eps < 0.f || !std::isfinite(out_eps) || out_eps < 0.f)
     return ATTN_RES_EINVAL;
-  int split = 0;
-  if (resolve_split(T, layout->flags, &split) != ATTN_RES_OK) return ATTN_RES_EINVAL;
-  if ((layout->flags & ~(ATTN_RES_FLAG_PDL | ATTN_RES_FLAG_SPLIT(0xff))) != 0) return ATTN_RES_EINVAL;
-  if (T * split > INT32_MAX) return ATTN_RES_EINVAL;
+  if ((layout->flags & ~kKnownFlags) != 0) return ATTN_RES_EINVAL;
+  Plan plan;
+  if (make_plan(T, layout->flags, &plan) != ATTN_RES_OK) return ATTN_RES_EINVAL;
+  if (T * plan.split > INT32_MAX) return ATTN_RES_EINVAL;
   // no rows: nothing is read or written, so pointers and strides do not matter
   if (T == 0) return ATTN_RES_OK;
 
@@ -205,8 +292,6 @@ attn_res_status_t attn_res(attn_res_bf16_t* prefix, const attn_res_bf16_t* delta
   int dev = 0;
   attn_res_status_t st = check_device(&dev);
   if (st != ATTN_RES_OK) return st;
-  LaunchFn fn = lookup(num_blocks, split_index(split), has_delta, has_onorm);
-  if (fn == nullptr) return ATTN_RES_EINVAL;
 
   Params p;
   p.prefix = prefix;
@@ -225,7 +310,18 @@ attn_res_status_t attn_res(attn_res_bf16_t* prefix, const attn_res_bf16_t* delta
   p.eps = eps;
   p.out_eps = out_eps;
   const bool pdl = (layout->flags & ATTN_RES_FLAG_PDL) != 0;
-  cudaError_t e = fn(p, T, pdl, static_cast<cudaStream_t>(stream), dev);
+  cudaError_t e = status_word(dev, &p.err);
+  if (e == cudaSuccess) {
+    if (plan.kernel == ATTN_RES_KERNEL_SPLIT) {
+      LaunchFn fn = lookup(num_blocks, split_index(plan.split), has_delta, has_onorm);
+      if (fn == nullptr) return ATTN_RES_EINVAL;
+      e = fn(p, T, pdl, static_cast<cudaStream_t>(stream), dev);
+    } else {
+      StreamLaunchFn fn = lookup_stream(num_blocks, plan.shape, has_delta, has_onorm);
+      if (fn == nullptr) return ATTN_RES_EINVAL;
+      e = fn(p, T, pdl, static_cast<cudaStream_t>(stream), dev);
+    }
+  }
   if (e != cudaSuccess) {
     (void)cudaGetLastError();
     return ATTN_RES_ECUDA;

@@ -32,4 +32,31 @@ LaunchFn ATTN_RES_CAT(launcher_s, ATTN_RES_S)(int split_idx, bool d, bool o) {
   }
 }
 
+namespace {
+template <int SH>
+StreamLaunchFn pick_stream(bool d, bool o) {
+  constexpr int S = ATTN_RES_S;
+  constexpr int K = kStreamShapes[SH].k;
+  constexpr int V = kStreamShapes[SH].vpt;
+  constexpr int ST = kStreamShapes[SH].stages;
+  if (d) return o ? &launch_stream<S, true, true, K, V, ST> : &launch_stream<S, true, false, K, V, ST>;
+  return o ? &launch_stream<S, false, true, K, V, ST> : &launch_stream<S, false, false, K, V, ST>;
+}
+}  // namespace
+
+StreamLaunchFn ATTN_RES_CAT(stream_launcher_s, ATTN_RES_S)(int shape_idx, bool d, bool o) {
+  static_assert(kNumStreamShapes == 8, "update the switch below");
+  switch (shape_idx) {
+    case 0: return pick_stream<0>(d, o);
+    case 1: return pick_stream<1>(d, o);
+    case 2: return pick_stream<2>(d, o);
+    case 3: return pick_stream<3>(d, o);
+    case 4: return pick_stream<4>(d, o);
+    case 5: return pick_stream<5>(d, o);
+    case 6: return pick_stream<6>(d, o);
+    case 7: return pick_stream<7>(d, o);
+    default: return nullptr;
+  }
+}
+
 }  // namespace attn_res_host

@@ -6,6 +6,7 @@
 #include <cstdint>
 
 #include "attn_res_kernel.cuh"
+#include "attn_res_stream.cuh"
 
 namespace attn_res_host {
 
@@ -65,6 +66,94 @@ cudaError_t launch_split(const Params& p, int64_t T, bool pdl,
   return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
+// Shapes the persistent stream kernel is built for: CTAs per token row (K),
+// 16-byte vectors per thread and per row (VPT), ring depth (STAGES).
+struct StreamShape {
+  int k, vpt, stages;
+};
+constexpr StreamShape kStreamShapes[] = {{7, 1, 2}, {7, 2, 2}, {7, 4, 2}, {4, 2, 2},
+                                         {4, 4, 2}, {4, 2, 3}, {14, 2, 2}, {2, 4, 2}};
+constexpr int kNumStreamShapes = sizeof(kStreamShapes) / sizeof(kStreamShapes[0]);
+
+inline int stream_shape_index(int k, int vpt, int stages) {
+  for (int i = 0; i < kNumStreamShapes; ++i)
+    if (kStreamShapes[i].k == k && kStreamShapes[i].vpt == vpt && kStreamShapes[i].stages == stages)
+      return i;
+  return -1;
+}
+
+// Enqueue the persistent kernel: as many clusters as fit on the device at
+// once (at most T), each streaming every ncl-th token.
+using StreamLaunchFn = cudaError_t (*)(const Params&, int64_t T, bool pdl,
+                                       cudaStream_t stream, int device);
+
+template <int S, bool D, bool O, int K, int VPT, int STAGES>
+cudaError_t launch_stream(const Params& p, int64_t T, bool pdl, cudaStream_t stream,
+                          int device) {
+  using C = attn_res_dev::StreamCfg<S, D, O, K, VPT, STAGES>;
+  void (*kern)(Params, int64_t) = attn_res_dev::attn_res_stream_kernel<S, D, O, K, VPT, STAGES>;
+  // per device: attributes set and the number of co-resident clusters
+  static std::atomic<int> clusters_per_device[64];
+  if (device < 0 || device >= 64) return cudaErrorInvalidDevice;
+  int ncl_max = clusters_per_device[device].load(std::memory_order_acquire);
+  if (ncl_max == 0) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    if (C::COMM && K > 8) {
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+      if (e != cudaSuccess) return e;
+    }
+    if (C::COMM) {
+      cudaLaunchAttribute a;
+      a.id = cudaLaunchAttributeClusterDimension;
+      a.val.clusterDim.x = K;
+      a.val.clusterDim.y = 1;
+      a.val.clusterDim.z = 1;
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(K * 1024, 1, 1);
+      cfg.blockDim = dim3(C::THREADS, 1, 1);
+      cfg.dynamicSmemBytes = C::SMEM_BYTES;
+      cfg.attrs = &a;
+      cfg.numAttrs = 1;
+      e = cudaOccupancyMaxActiveClusters(&ncl_max, kern, &cfg);
+      if (e != cudaSuccess) return e;
+    } else {
+      int per_sm = 0, sms = 0;
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, C::THREADS, C::SMEM_BYTES);
+      if (e != cudaSuccess) return e;
+      e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
+      if (e != cudaSuccess) return e;
+      ncl_max = per_sm * sms / K;
+    }
+    if (ncl_max < 1) return cudaErrorInvalidConfiguration;
+    clusters_per_device[device].store(ncl_max, std::memory_order_release);
+  }
+  const int64_t ncl = T < ncl_max ? T : ncl_max;
+  cudaLaunchAttribute attrs[2];
+  unsigned n = 0;
+  if (C::COMM) {
+    attrs[n].id = cudaLaunchAttributeClusterDimension;
+    attrs[n].val.clusterDim.x = K;
+    attrs[n].val.clusterDim.y = 1;
+    attrs[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  if (pdl) {
+    attrs[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attrs[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(ncl * K), 1, 1);
+  cfg.blockDim = dim3(C::THREADS, 1, 1);
+  cfg.dynamicSmemBytes = C::SMEM_BYTES;
+  cfg.stream = stream;
+  cfg.attrs = attrs;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, kern, p, T);
+}
+
 // One row of the table per num_blocks, defined in attn_res_inst.cu (compiled
 // once per S).  Returns nullptr for an unknown split index.
 LaunchFn launcher_s0(int split_idx, bool has_delta, bool has_onorm);
@@ -76,5 +165,15 @@ LaunchFn launcher_s5(int split_idx, bool has_delta, bool has_onorm);
 LaunchFn launcher_s6(int split_idx, bool has_delta, bool has_onorm);
 LaunchFn launcher_s7(int split_idx, bool has_delta, bool has_onorm);
 LaunchFn launcher_s8(int split_idx, bool has_delta, bool has_onorm);
+
+StreamLaunchFn stream_launcher_s0(int shape_idx, bool d, bool o);
+StreamLaunchFn stream_launcher_s1(int shape_idx, bool d, bool o);
+StreamLaunchFn stream_launcher_s2(int shape_idx, bool d, bool o);
+StreamLaunchFn stream_launcher_s3(int shape_idx, bool d, bool o);
+StreamLaunchFn stream_launcher_s4(int shape_idx, bool d, bool o);
+StreamLaunchFn stream_launcher_s5(int shape_idx, bool d, bool o);
+StreamLaunchFn stream_launcher_s6(int shape_idx, bool d, bool o);
+StreamLaunchFn stream_launcher_s7(int shape_idx, bool d, bool o);
+StreamLaunchFn stream_launcher_s8(int shape_idx, bool d, bool o);
 
 }  // namespace attn_res_host

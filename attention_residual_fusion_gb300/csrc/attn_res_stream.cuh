@@ -1,0 +1,202 @@
+// attn_res_stream.cuh -- persistent, TMA-fed kernel for many tokens.
+//
+// Same column split and per-token arithmetic as the split kernel (one cluster
+// of K CTAs per token row, CTA r owning a contiguous 1/K of every row, see
+// attn_res_token.cuh), but each cluster loops over many tokens and keeps the
+// HBM stream going while it reduces:
+//
+//   * thread 0 of each CTA issues bulk copies (cp.async.bulk, the TMA
+//     engine's one-dimensional form) of the CTA's slice of every source row of
+//     a token into one stage of a STAGES-deep shared-memory ring; the copies
+//     complete on the stage's `full` mbarrier (expect-tx of the stage's bytes);
+//   * every thread waits on `full` (bounded: on time-out the kernel records an
+//     error bit, stops issuing copies and runs to completion) and reads its VPT
+//     vectors of every row straight from the stage, once for the partial sums
+//     and once for the mix -- rows are not copied into registers, which keeps
+//     the register footprint per token small and lets more clusters run;
+//   * after its last read of the stage each warp arrives on the stage's
+//     `empty` mbarrier; thread 0 waits on it, fences the generic-proxy reads
+//     against the async proxy, and refills the stage with the token STAGES
+//     ahead.
+//
+// Staging rows in shared memory with TMA and mbarriers follows the design of
+// the kernel excerpted in the prhub summaries of vllm PR #54261 and #50185;
+// the pages chunk sources with an online softmax, here a stage holds all
+// sources of one token slice and the softmax is taken once.
+#pragma once
+
+#include "attn_res_token.cuh"
+
+namespace attn_res_dev {
+
+template <int S, bool HAS_DELTA, bool HAS_ONORM, int K, int VPT, int STAGES>
+struct StreamCfg {
+  static constexpr int VPC = kNV / K;                      // vectors per CTA per row
+  static constexpr int THREADS = (VPC / VPT + 31) / 32 * 32;
+  static constexpr int NW = THREADS / 32;
+  using Tok = TokenCfg<S, HAS_DELTA, HAS_ONORM, K, NW>;
+  static constexpr int ROWS = Tok::ROWS;  // bank rows, prefix, delta
+  static constexpr bool COMM = Tok::COMM;
+  static constexpr uint32_t SLICE_BYTES = VPC * 16;  // one row's slice, multiple of 16
+  static constexpr uint32_t STAGE_BYTES = ROWS * SLICE_BYTES;
+  static constexpr uint32_t SMEM_BYTES = STAGES * STAGE_BYTES;
+  static_assert(kNV % K == 0, "split must divide the 896 row vectors");
+  static_assert(VPC % VPT == 0, "vectors per thread must divide the slice");
+  static_assert(STAGES >= 2 && STAGES <= 4, "ring depth");
+};
+
+template <int S, bool HAS_DELTA, bool HAS_ONORM, int K, int VPT, int STAGES>
+__global__ void __launch_bounds__(StreamCfg<S, HAS_DELTA, HAS_ONORM, K, VPT, STAGES>::THREADS)
+    attn_res_stream_kernel(const Params p, const int64_t T) {
+  using C = StreamCfg<S, HAS_DELTA, HAS_ONORM, K, VPT, STAGES>;
+  using Tok = typename C::Tok;
+  constexpr int ROWS = C::ROWS;
+  constexpr int VPC = C::VPC;
+  constexpr int THREADS = C::THREADS;
+  constexpr int NW = C::NW;
+  constexpr bool COMM = C::COMM;
+
+  extern __shared__ __align__(128) uint4 ring[];  // [STAGES][ROWS][VPC]
+  __shared__ __align__(8) unsigned long long full_bar[STAGES];
+  __shared__ __align__(8) unsigned long long empty_bar[STAGES];
+  __shared__ typename Tok::Box mb;
+
+  const int tid = threadIdx.x;
+  const int lane = tid & 31;
+  const int warp = tid >> 5;
+  const uint32_t rank = COMM ? cluster_ctarank() : (blockIdx.x % K);
+  const int64_t cid = blockIdx.x / K;  // cluster (token group) index
+  const int64_t ncl = gridDim.x / K;   // clusters in the grid
+  const int64_t ntok = (T > cid) ? (T - cid + ncl - 1) / ncl : 0;
+  const int64_t slice0 = (int64_t)rank * VPC * kVec;  // first column of this CTA
+  const uint32_t ring_addr = smem_addr(ring);
+  // vector v of this thread: index tid + v * THREADS within the CTA's slice
+  bool active[VPT];
+#pragma unroll
+  for (int v = 0; v < VPT; ++v) active[v] = tid + v * THREADS < VPC;
+
+  if (tid == 0) {
+#pragma unroll
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(smem_addr(&full_bar[s]), 1);
+      mbar_init(smem_addr(&empty_bar[s]), NW);
+    }
+    if (COMM) mailbox_init(mb);
+    fence_mbar_init();
+  }
+  if (COMM) {
+    cluster_arrive_release();  // matched by the wait before the first remote store
+  } else {
+    __syncthreads();
+  }
+
+  // producer side (thread 0): copies of one token into one stage
+  auto stage_dst = [&](int s, int row) -> uint32_t {
+    return ring_addr + (uint32_t)(s * ROWS + row) * C::SLICE_BYTES;
+  };
+  auto issue_bank = [&](int64_t t, int s) {
+    const uint32_t bar = smem_addr(&full_bar[s]);
+    mbar_arrive_expect_tx(bar, C::STAGE_BYTES);
+    const uint16_t* bp = p.blocks + t * p.blocks_token + slice0;
+#pragma unroll
+    for (int i = 0; i < S; ++i)
+      bulk_load(stage_dst(s, i), bp + (int64_t)i * p.blocks_slot, C::SLICE_BYTES, bar);
+  };
+  auto issue_current = [&](int64_t t, int s) {
+    const uint32_t bar = smem_addr(&full_bar[s]);
+    bulk_load(stage_dst(s, S), p.prefix + t * p.prefix_row + slice0, C::SLICE_BYTES, bar);
+    if (HAS_DELTA)
+      bulk_load(stage_dst(s, S + 1), p.delta + t * p.delta_row + slice0, C::SLICE_BYTES, bar);
+  };
+
+  // prologue: bank rows of the first STAGES tokens before the grid-dependency
+  // wait, prefix and delta after it.  Thread 0 also tracks the stages whose
+  // last issued copies it has not yet seen complete, and that issue's parity.
+  uint32_t pending = 0, pending_parity = 0;
+  if (tid == 0) {
+    for (int s = 0; s < STAGES && s < ntok; ++s) issue_bank(cid + s * ncl, s);
+  }
+  // weights: read-only, independent of the preceding kernel
+  uint4 rw[VPT], qw[VPT], ow[VPT];
+#pragma unroll
+  for (int v = 0; v < VPT; ++v) {
+    rw[v] = qw[v] = ow[v] = make_uint4(0, 0, 0, 0);
+    if (active[v]) {
+      const int64_t col = slice0 + (int64_t)(tid + v * THREADS) * kVec;
+      rw[v] = ld_weight(p.rms_w + col);
+      qw[v] = ld_weight(p.res_w + col);
+      if (HAS_ONORM) ow[v] = ld_weight(p.onw + col);
+    }
+  }
+  grid_dep_wait();  // every thread: also orders our stores after the producer's work
+  if (tid == 0) {
+    for (int s = 0; s < STAGES && s < ntok; ++s) {
+      issue_current(cid + s * ncl, s);
+      pending |= 1u << s;  // first use of every stage: parity 0
+    }
+  }
+  grid_dep_launch_dependents();
+
+  f32x2 q[VPT][4];
+  make_query<VPT>(rw, qw, q);
+  if (COMM) cluster_wait_acquire();
+
+  bool failed = false;
+  for (int64_t j = 0; j < ntok; ++j) {
+    const int s = (int)(j % STAGES);
+    const uint32_t sparity = (uint32_t)((j / STAGES) & 1);
+    const int b = (int)(j & 1);                         // mailbox buffer
+    const uint32_t bparity = (uint32_t)((j >> 1) & 1);  // its phase parity
+    const int64_t t = cid + j * ncl;
+    if (COMM && tid == 0) mailbox_expect<Tok>(mb, b, HAS_ONORM);
+
+    const bool was_failed = failed;
+    wait_or_flag(smem_addr(&full_bar[s]), sparity, failed, p.err, kErrStageTimeout);
+    if (tid == 0 && !was_failed && !failed) pending &= ~(1u << s);
+
+    const uint4* stage = ring + s * ROWS * VPC + tid;
+    auto row = [&](int i, int v) -> uint4 {
+      return active[v] ? stage[i * VPC + v * THREADS] : make_uint4(0, 0, 0, 0);
+    };
+    auto release = [&]() {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_addr(&empty_bar[s]));
+    };
+    uint4 c[VPT], o[VPT];
+    mix_token<S, HAS_DELTA, HAS_ONORM, K, NW, VPT>(row, q, ow, mb, b, bparity, rank, warp, lane,
+                                                    p.eps, p.out_eps, failed, p.err, release, c, o);
+#pragma unroll
+    for (int v = 0; v < VPT; ++v) {
+      if (active[v]) {
+        const int64_t col = slice0 + (int64_t)(tid + v * THREADS) * kVec;
+        st_row(p.out + t * p.out_row + col, o[v]);
+        if (HAS_DELTA) st_row(p.prefix + t * p.prefix_row + col, c[v]);
+        if (p.write_idx >= 0)
+          st_row(p.blocks + t * p.blocks_token + (int64_t)p.write_idx * p.blocks_slot + col, c[v]);
+      }
+    }
+
+    // refill stage s with the token STAGES ahead, once every local warp is
+    // done with it
+    if (tid == 0 && !failed && j + STAGES < ntok) {
+      wait_or_flag(smem_addr(&empty_bar[s]), sparity, failed, p.err, kErrStageTimeout);
+      if (!failed) {
+        fence_proxy_async_smem();
+        const int64_t tn = cid + (j + STAGES) * ncl;
+        issue_bank(tn, s);
+        issue_current(tn, s);
+        pending |= 1u << s;
+        pending_parity = (pending_parity & ~(1u << s)) | ((sparity ^ 1u) << s);
+      }
+    }
+  }
+
+  // After a time-out, do not leave with copies still landing in shared memory.
+  if (tid == 0 && failed) {
+    for (int s = 0; s < STAGES; ++s)
+      if (pending & (1u << s))
+        (void)mbar_wait_bounded(smem_addr(&full_bar[s]), (pending_parity >> s) & 1u);
+  }
+}
+
+}  // namespace attn_res_dev

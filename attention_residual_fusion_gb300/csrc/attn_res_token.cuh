@@ -1,0 +1,203 @@
+// attn_res_token.cuh -- the mixture for one token, as seen by one thread
+// that owns VPT 16-byte vectors (8 columns each) of every source row; shared
+// by the split and the stream kernels.
+//
+// Per token (implementation walkthrough of vllm-ascend PR #14840; delta
+// packing and output norm from the key source excerpts of vllm PR #54261):
+//   c = bf16_rn(prefix + delta); per source i: ss_i = sum x^2, dt_i = <x, q>;
+//   l_i = dt_i / sqrt(ss_i / H + eps); w = softmax(l); acc = sum_i w_i x_i;
+//   optional out = acc / sqrt(mean(acc^2) + out_eps) * w_out.
+//
+// The full-row sums cross the K CTAs of the cluster through mailboxes in
+// shared memory: every warp reduces its partial sums (reduce-scatter), and
+// the lanes holding them store each one into the mailbox of every CTA of the
+// cluster with st.async, which completes transaction bytes on the receiver's
+// mbarrier.  A warp waits on its own CTA's mbarrier until all K x NW partial
+// vectors have landed, then sums them in a fixed order -- so every warp of
+// every CTA of the token computes bit-identical logits and weights, with no
+// CTA barrier, no cluster barrier and no memory fence on the way.
+// Elementwise products use packed fp32 pairs (fma.rn.f32x2).
+#pragma once
+
+#include "attn_res_common.cuh"
+
+namespace attn_res_dev {
+
+// Mailboxes of one CTA, double-buffered by token parity (a peer may run one
+// token ahead; it cannot run two ahead, since it needs this CTA's sums of the
+// token in between).
+template <int K, int NW, int NR>
+struct Mailbox {
+  float sums[2][K * NW][NR];  // per source CTA and warp: ss_0..ss_S, dt_0..dt_S
+  float sq[2][K * NW];        // per source CTA and warp: sum of acc^2
+  unsigned long long bar_sums[2];
+  unsigned long long bar_sq[2];
+};
+
+template <int S, bool HAS_DELTA, bool HAS_ONORM, int K, int NW>
+struct TokenCfg {
+  static constexpr int N = S + 1;              // sources
+  static constexpr int NR = 2 * N;             // partial sums per token
+  static constexpr int ROWS = N + (HAS_DELTA ? 1 : 0);
+  static constexpr int P = pow2_at_least(NR);  // padded for the reduce-scatter
+  static constexpr int SHIFT = 5 - log2_exact(P);
+  static constexpr uint32_t SUMS_BYTES = K * NW * NR * 4;  // expected per token
+  static constexpr uint32_t SQ_BYTES = K * NW * 4;
+  static constexpr bool COMM = (S > 0) || HAS_ONORM;
+  using Box = Mailbox<K, NW, NR>;
+  static_assert(K * NW <= 32, "one lane per mailbox slot");
+};
+
+// Initialise the mailbox barriers (thread 0 of the CTA).
+template <class Box>
+__device__ __forceinline__ void mailbox_init(Box& mb) {
+  for (int b = 0; b < 2; ++b) {
+    mbar_init(smem_addr(&mb.bar_sums[b]), 1);
+    mbar_init(smem_addr(&mb.bar_sq[b]), 1);
+  }
+}
+
+// Thread 0, once per token before waiting: the one arrival of this phase,
+// with the byte count the peers' stores will complete.
+template <class Cfg>
+__device__ __forceinline__ void mailbox_expect(typename Cfg::Box& mb, int b, bool has_onorm) {
+  if (Cfg::N > 1) mbar_arrive_expect_tx(smem_addr(&mb.bar_sums[b]), Cfg::SUMS_BYTES);
+  if (has_onorm) mbar_arrive_expect_tx(smem_addr(&mb.bar_sq[b]), Cfg::SQ_BYTES);
+}
+
+// q = rms_w * res_w for the thread's columns, as fp32 pairs.
+template <int VPT>
+__device__ __forceinline__ void make_query(const uint4 (&rw)[VPT], const uint4 (&qw)[VPT],
+                                           f32x2 (&q)[VPT][4]) {
+#pragma unroll
+  for (int v = 0; v < VPT; ++v)
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      q[v][k] = f2_mul(bf2_widen(vword(rw[v], k)), bf2_widen(vword(qw[v], k)));
+}
+
+// row(i, v): vector v of row i (bank rows 0..S-1, prefix S, delta S+1);
+// zeros for idle threads.  after_mix(): called once the thread no longer
+// needs any row data of this token.  b / parity: mailbox buffer and its phase
+// parity for this token.  Writes c (current-layer row) and out.
+template <int S, bool HAS_DELTA, bool HAS_ONORM, int K, int NW, int VPT, class Row,
+          class AfterMix>
+__device__ __forceinline__ void mix_token(Row row, const f32x2 (&q)[VPT][4],
+                                          const uint4 (&ow)[VPT],
+                                          typename TokenCfg<S, HAS_DELTA, HAS_ONORM, K, NW>::Box& mb,
+                                          int b, uint32_t parity, uint32_t rank, int warp,
+                                          int lane, float eps, float out_eps, bool& failed,
+                                          unsigned* err, AfterMix after_mix, uint4 (&c)[VPT],
+                                          uint4 (&out)[VPT]) {
+  using C = TokenCfg<S, HAS_DELTA, HAS_ONORM, K, NW>;
+  constexpr int N = C::N;
+  constexpr int NR = C::NR;
+  constexpr int P = C::P;
+  const int src = (int)rank * NW + warp;  // this warp's slot in every mailbox
+
+#pragma unroll
+  for (int v = 0; v < VPT; ++v) {
+    if constexpr (HAS_DELTA) {
+      c[v] = add_bf16x8(row(S, v), row(S + 1, v));
+    } else {
+      c[v] = row(S, v);
+    }
+  }
+
+  f32x2 acc[VPT][4];
+  if constexpr (S == 0) {
+#pragma unroll
+    for (int v = 0; v < VPT; ++v)
+#pragma unroll
+      for (int k = 0; k < 4; ++k) acc[v][k] = bf2_widen(vword(c[v], k));
+    after_mix();
+  } else {
+    // per-source partial sums over this thread's columns
+    float part[P];
+#pragma unroll
+    for (int r = 0; r < P; ++r) part[r] = 0.f;
+#pragma unroll
+    for (int i = 0; i < N; ++i) {
+      f32x2 ss = 0ull, dt = 0ull;  // +0.0f pairs
+#pragma unroll
+      for (int v = 0; v < VPT; ++v) {
+        const uint4 xi = (i < S) ? row(i < S ? i : 0, v) : c[v];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const f32x2 x2 = bf2_widen(vword(xi, k));
+          ss = f2_fma(x2, x2, ss);
+          dt = f2_fma(x2, q[v][k], dt);
+        }
+      }
+      part[i] = f2_lo(ss) + f2_hi(ss);
+      part[N + i] = f2_lo(dt) + f2_hi(dt);
+    }
+    // warp totals, then into every CTA's mailbox
+    const float tv = reduce_scatter<P>(part, lane);
+    const int idx = lane >> C::SHIFT;
+    if ((lane & ((1 << C::SHIFT) - 1)) == 0 && idx < NR) {
+      const uint32_t a = smem_addr(&mb.sums[b][src][idx]);
+      const uint32_t bar = smem_addr(&mb.bar_sums[b]);
+#pragma unroll
+      for (int r = 0; r < K; ++r) st_async_f32(map_rank(a, r), tv, map_rank(bar, r));
+    }
+    wait_or_flag(smem_addr(&mb.bar_sums[b]), parity, failed, err, kErrExchangeTimeout);
+    // token totals in a fixed order, logits and softmax (every warp)
+    float tot = 0.f;
+    if (lane < NR) {
+#pragma unroll 4
+      for (int s = 0; s < K * NW; ++s) tot += mb.sums[b][s][lane];
+    }
+    const float dtv = __shfl_sync(0xffffffffu, tot, (lane + N) & 31);
+    float logit = __int_as_float(0xff800000u);  // -inf
+    if (lane < N) logit = dtv / sqrtf(tot / (float)kH + eps);
+    const float m = warp_max(logit);
+    const float e = (lane < N) ? expf(logit - m) : 0.f;
+    const float z = warp_sum(e);
+    const float wl = e / z;
+#pragma unroll
+    for (int v = 0; v < VPT; ++v)
+#pragma unroll
+      for (int k = 0; k < 4; ++k) acc[v][k] = 0ull;
+#pragma unroll
+    for (int i = 0; i < N; ++i) {
+      const float w = __shfl_sync(0xffffffffu, wl, i);
+      const f32x2 w2 = f2_make(w, w);
+#pragma unroll
+      for (int v = 0; v < VPT; ++v) {
+        const uint4 xi = (i < S) ? row(i < S ? i : 0, v) : c[v];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) acc[v][k] = f2_fma(w2, bf2_widen(vword(xi, k)), acc[v][k]);
+      }
+    }
+    after_mix();
+  }
+
+  if constexpr (HAS_ONORM) {
+    f32x2 sq2 = 0ull;
+#pragma unroll
+    for (int v = 0; v < VPT; ++v)
+#pragma unroll
+      for (int k = 0; k < 4; ++k) sq2 = f2_fma(acc[v][k], acc[v][k], sq2);
+    const float sq = warp_sum(f2_lo(sq2) + f2_hi(sq2));
+    if (lane < K)
+      st_async_f32(map_rank(smem_addr(&mb.sq[b][src]), lane), sq,
+                   map_rank(smem_addr(&mb.bar_sq[b]), lane));
+    wait_or_flag(smem_addr(&mb.bar_sq[b]), parity, failed, err, kErrExchangeTimeout);
+    const float tot = warp_sum(lane < K * NW ? mb.sq[b][lane] : 0.f);
+    const float ro = 1.0f / sqrtf(tot / (float)kH + out_eps);
+    const f32x2 ro2 = f2_make(ro, ro);
+#pragma unroll
+    for (int v = 0; v < VPT; ++v)
+#pragma unroll
+      for (int k = 0; k < 4; ++k) acc[v][k] = f2_mul(f2_mul(acc[v][k], ro2), bf2_widen(vword(ow[v], k)));
+  }
+#pragma unroll
+  for (int v = 0; v < VPT; ++v)
+    out[v] = make_uint4(pack_bf16x2(f2_lo(acc[v][0]), f2_hi(acc[v][0])),
+                        pack_bf16x2(f2_lo(acc[v][1]), f2_hi(acc[v][1])),
+                        pack_bf16x2(f2_lo(acc[v][2]), f2_hi(acc[v][2])),
+                        pack_bf16x2(f2_lo(acc[v][3]), f2_hi(acc[v][3])));
+}
+
+}  // namespace attn_res_dev

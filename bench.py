@@ -192,21 +192,24 @@ def device_tensors(wl, torch, dev):
                 out=torch.empty((wl.T, wl.H), dtype=torch.bfloat16, device=dev))
 
 
-def call(ar, wl, t, stream, split=0, pdl=False):
+TUNE = dict(split=0, kernel=0, stages=0, vpt=0)  # launch overrides from the command line
+
+
+def call(ar, wl, t, stream, pdl=False):
     ar.attn_res(t["prefix"], t["delta"], t["bank"][:, :, : wl.H], wl.num_blocks,
                 wl.block_write_idx, t["res"], t["rms"], t["onw"], wl.eps, wl.out_eps,
-                t["out"], split=split, pdl=pdl, stream=stream)
+                t["out"], pdl=pdl, stream=stream, **TUNE)
 
 
-def time_device(ar, wl, t, torch, stream, steps, warmup, split=0):
+def time_device(ar, wl, t, torch, stream, steps, warmup):
     for _ in range(warmup):
-        call(ar, wl, t, stream, split)
+        call(ar, wl, t, stream)
     torch.cuda.synchronize()
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
     with torch.cuda.stream(stream):
         ev[0].record(stream)
         for i in range(steps):
-            call(ar, wl, t, stream, split)
+            call(ar, wl, t, stream)
             ev[i + 1].record(stream)
     torch.cuda.synchronize()
     per = [ev[i].elapsed_time(ev[i + 1]) for i in range(steps)]
@@ -320,17 +323,19 @@ def run_ours(args, rank, world, local_rank, dist):
     wl, desc = make(args.workload)
     t = device_tensors(wl, torch, dev)
     stream = torch.cuda.Stream(dev)
+    TUNE.update(split=args.split, kernel=args.kernel, stages=args.stages, vpt=args.vpt)
     shape = ar.launch_shape(wl.T, wl.num_blocks, wl.out_norm_w is not None,
-                            ar.FLAG_SPLIT(args.split))
+                            ar.FLAG_SPLIT(args.split) | ar.FLAG_KERNEL(args.kernel) |
+                            ar.FLAG_STAGES(args.stages) | ar.FLAG_VPT(args.vpt))
 
     for _ in range(max(args.warmup, 3)):
-        call(ar, wl, t, stream, args.split)
+        call(ar, wl, t, stream)
     torch.cuda.synchronize()
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
     with ClockSampler(local_rank) as clk:
-        total_ms, per = time_device(ar, wl, t, torch, stream, args.steps, 0, args.split)
+        total_ms, per = time_device(ar, wl, t, torch, stream, args.steps, 0)
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
@@ -365,7 +370,7 @@ def run_ours(args, rank, world, local_rank, dist):
                      "algorithmic_bytes_per_launch": alg_bytes,
                      "mean_launch_us": round(mean_launch_ms * 1e3, 3),
                      "traffic": recorded_traffic(args.workload),
-                     "kernel": "attn_res_split_kernel"},
+                     "kernel": f"attn_res_{shape['kernel']}_kernel"},
         "gpu_launches": args.steps,
         "clocks": clk.summary(),
     }
@@ -435,6 +440,9 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="long_prefill")
     ap.add_argument("--split", type=int, default=0, help="CTAs per token row (0 = automatic)")
+    ap.add_argument("--kernel", type=int, default=0, help="1 split, 2 stream (0 = automatic)")
+    ap.add_argument("--stages", type=int, default=0, help="stream kernel ring depth (0 = automatic)")
+    ap.add_argument("--vpt", type=int, default=0, help="16-byte vectors per thread (0 = automatic)")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--ref-budget", type=float, default=60.0)

@@ -65,10 +65,24 @@ typedef enum {
  * the wait: PDL discipline in the key source excerpts of vllm PR #54261. */
 #define ATTN_RES_FLAG_PDL 0x1u
 
-/* Tuning override: the number of CTAs (one thread-block cluster) a token row
- * is split over.  0 = automatic.  Accepted: 4, 7, 8, 14, 16.  Results do not
- * depend on it beyond fp32 summation order. */
+/* Tuning overrides (0 = automatic).  Results do not depend on them beyond
+ * fp32 summation order.
+ *   SPLIT(k):  CTAs (one thread-block cluster) a token row is split over;
+ *              split kernel 4, 7, 8, 14 or 16; stream kernel see below.
+ *   KERNEL(k): ATTN_RES_KERNEL_SPLIT -- one cluster per token row, rows held
+ *              in registers (latency path for few tokens);
+ *              ATTN_RES_KERNEL_STREAM -- persistent clusters that stream many
+ *              tokens through a TMA-filled shared-memory ring.
+ *   STAGES(n): ring depth of the stream kernel.
+ *   VPT(n):    16-byte vectors per thread and row (split kernel: 1).
+ * Stream kernel shapes (split, vpt, stages): (7,1,2) (7,2,2) (7,4,2) (4,2,2)
+ * (4,4,2) (4,2,3) (14,2,2) (2,4,2); unset fields default to 4, 2 and 2. */
 #define ATTN_RES_FLAG_SPLIT(k) (((uint32_t)(k) & 0xffu) << 8)
+#define ATTN_RES_FLAG_KERNEL(k) (((uint32_t)(k) & 0xfu) << 16)
+#define ATTN_RES_FLAG_STAGES(n) (((uint32_t)(n) & 0xfu) << 20)
+#define ATTN_RES_FLAG_VPT(n) (((uint32_t)(n) & 0xfu) << 24)
+#define ATTN_RES_KERNEL_SPLIT 1
+#define ATTN_RES_KERNEL_STREAM 2
 
 /* Memory layout of the tensors, in elements.  A row is H contiguous
  * elements; columns H .. stride-1 are padding that is never read or
@@ -136,16 +150,30 @@ int attn_res_max_blocks(void);
 
 /*
  * attn_res_launch_shape -- the launch attn_res would make for T rows with
- * num_blocks sources, output norm on/off and the given flags: CTAs per token
- * row (`split`, 1 when the CTAs need not talk to each other), threads per
- * CTA, CTAs in the grid and the thread-block cluster size (1 = no cluster).
+ * num_blocks sources, output norm on/off and the given flags: the kernel
+ * (ATTN_RES_KERNEL_*), CTAs per token row (`split`), ring depth (`stages`, 0
+ * for the split kernel), threads per CTA, CTAs in the grid (0 for the stream
+ * kernel, whose grid is as many clusters as fit on the device, at most T) and
+ * the thread-block cluster size (1 when the CTAs of a row never exchange
+ * sums: no bank rows and no output norm).  Any output pointer may be NULL.
  * Pure host computation, no CUDA call.  Returns ATTN_RES_EINVAL for T < 0,
- * num_blocks outside 0..8 or an unsupported split override.
+ * num_blocks outside 0..8 or an unsupported override.
  */
 attn_res_status_t attn_res_launch_shape(int64_t T, int num_blocks,
                                         int has_out_norm, uint32_t flags,
-                                        int* split, int* threads_per_cta,
-                                        int64_t* ctas, int* cluster);
+                                        int* kernel, int* split, int* stages,
+                                        int* threads_per_cta, int64_t* ctas,
+                                        int* cluster);
+
+/*
+ * attn_res_device_status -- error bits the kernels recorded on the current
+ * device since the last clear (0 = none).  Bit 0: a wait for a shared-memory
+ * stage of row data timed out; bit 1: a wait for the partial sums of another
+ * CTA of the cluster timed out.  The kernel then finished without waiting
+ * further and that call's outputs are not valid.  With `clear` != 0 the word is reset.  Synchronous
+ * (cudaMemcpy); a diagnostic, not for the hot path.
+ */
+attn_res_status_t attn_res_device_status(unsigned int* bits, int clear);
 
 #ifdef __cplusplus
 }

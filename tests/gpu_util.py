@@ -31,8 +31,8 @@ class Guarded:
         return bool(np.all(a[:GUARD] == GUARD_BITS) and np.all(a[-GUARD:] == GUARD_BITS))
 
 
-def run_gpu(wl: W.Workload, *, split: int = 0, pdl: bool = False,
-            prefix_row: int | None = None, out_row: int | None = None):
+def run_gpu(wl: W.Workload, *, split: int = 0, pdl: bool = False, kernel: int = 0,
+            stages: int = 0, vpt: int = 0, prefix_row: int | None = None, out_row: int | None = None):
     """Copy the workload to the device (guarded), call attn_res through the C
     ABI, and return host copies of out, prefix and the bank."""
     import torch
@@ -52,7 +52,8 @@ def run_gpu(wl: W.Workload, *, split: int = 0, pdl: bool = False,
     out = ar.attn_res(g_prefix.view[:, :H], None if g_delta is None else g_delta.view,
                       g_bank.view[:, :, :H], wl.num_blocks, wl.block_write_idx,
                       g_res.view, g_rms.view, None if g_onw is None else g_onw.view,
-                      wl.eps, wl.out_eps, g_out.view[:, :H], pdl=pdl, split=split)
+                      wl.eps, wl.out_eps, g_out.view[:, :H], pdl=pdl, split=split,
+                      kernel=kernel, stages=stages, vpt=vpt)
     torch.cuda.synchronize()
     bufs = [g for g in (g_prefix, g_delta, g_bank, g_rms, g_res, g_onw, g_out) if g is not None]
     assert all(g.guards_intact() for g in bufs), "a guard zone was written"

@@ -42,16 +42,29 @@ def test_constants(lib):
 
 
 def test_launch_shape(lib):
-    assert ar.launch_shape(1, 4, True) == dict(split=8, threads=128, ctas=8, cluster=8)
-    assert ar.launch_shape(1024, 8, False) == dict(split=7, threads=128, ctas=7168, cluster=7)
+    ls = ar.launch_shape
+    assert ls(1, 4, True) == dict(kernel="split", split=8, stages=0, threads=128, ctas=8, cluster=8)
+    assert ls(64, 8, False) == dict(kernel="split", split=7, stages=0, threads=128, ctas=448, cluster=7)
+    assert ls(8192, 8, True) == dict(kernel="stream", split=4, stages=2, threads=128, ctas=0, cluster=4)
     # no softmax and no output norm: the CTAs of a token never talk
-    assert ar.launch_shape(1024, 0, False)["cluster"] == 1
-    assert ar.launch_shape(2, 8, True, ar.FLAG_SPLIT(16)) == dict(split=16, threads=64, ctas=32, cluster=16)
-    assert ar.launch_shape(2, 8, True, ar.FLAG_SPLIT(4))["threads"] == 224
-    assert ar.launch_shape(2, 8, True, ar.FLAG_SPLIT(14))["threads"] == 64
-    for bad in [(-1, 0, 0, 0), (1, 9, 0, 0), (1, -1, 0, 0), (1, 1, 0, ar.FLAG_SPLIT(5))]:
+    assert ls(1024, 0, False)["cluster"] == 1
+    assert ls(2, 8, True, ar.FLAG_SPLIT(16)) == dict(kernel="split", split=16, stages=0, threads=64, ctas=32, cluster=16)
+    assert ls(2, 8, True, ar.FLAG_SPLIT(4))["threads"] == 224
+    assert ls(2, 8, True, ar.FLAG_SPLIT(14))["threads"] == 64
+    assert ls(2, 8, True, ar.FLAG_KERNEL(2) | ar.FLAG_SPLIT(4) | ar.FLAG_VPT(2) | ar.FLAG_STAGES(3))["stages"] == 3
+    assert ls(9000, 8, True, ar.FLAG_KERNEL(1))["kernel"] == "split"
+    assert ls(9000, 8, True, ar.FLAG_SPLIT(7) | ar.FLAG_VPT(2))["threads"] == 64
+    assert ls(9000, 8, True, ar.FLAG_SPLIT(7) | ar.FLAG_VPT(1))["threads"] == 128
+    for bad in [(-1, 0, 0, 0), (1, 9, 0, 0), (1, -1, 0, 0), (1, 1, 0, ar.FLAG_SPLIT(5)),
+                (1, 1, 0, ar.FLAG_KERNEL(3)), (1, 1, 0, ar.FLAG_KERNEL(2) | ar.FLAG_SPLIT(16)),
+                (1, 1, 0, ar.FLAG_KERNEL(2) | ar.FLAG_STAGES(4)),
+                (1, 1, 0, ar.FLAG_KERNEL(2) | ar.FLAG_SPLIT(8) | ar.FLAG_VPT(2)),
+                (1, 1, 0, ar.FLAG_KERNEL(2) | ar.FLAG_STAGES(4)),
+                (1, 1, 0, ar.FLAG_KERNEL(2) | ar.FLAG_SPLIT(7) | ar.FLAG_STAGES(3)),
+                (1, 1, 0, ar.FLAG_KERNEL(1) | ar.FLAG_VPT(2)),
+                (1, 1, 0, ar.FLAG_KERNEL(1) | ar.FLAG_STAGES(2)), (1, 1, 0, 1 << 30)]:
         with pytest.raises(ar.AttnResError):
-            ar.launch_shape(*bad)
+            ls(*bad)
 
 
 # Fake, well separated, 16-byte aligned device addresses: validation happens
@@ -138,6 +151,7 @@ def test_append_slot_equal_to_capacity_is_rejected(lib):
     ("blocks_slot", H - 8, 1), ("blocks_token", 7 * H, 1),
     ("prefix_row", H + 4, 2), ("blocks_slot", 7232 + 4, 2), ("out_row", H + 1, 2),
     ("blocks_capacity", -1, 1), ("flags", 0x4, 1), ("flags", ar.FLAG_SPLIT(5), 1),
+    ("flags", ar.FLAG_KERNEL(7), 1), ("flags", ar.FLAG_KERNEL(2) | ar.FLAG_SPLIT(16), 1),
 ])
 def test_layout_rejections(lib, field, value, status):
     kw = good()

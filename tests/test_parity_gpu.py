@@ -180,3 +180,43 @@ def test_repeated_calls_are_deterministic():
     a = G.run_gpu(wl)["out"]
     b = G.run_gpu(wl)["out"]
     assert np.array_equal(a, b)
+
+
+# ---- the persistent stream kernel ------------------------------------------------
+
+SHAPES = [(7, 1, 2), (7, 2, 2), (7, 4, 2), (4, 2, 2), (4, 4, 2), (4, 2, 3), (14, 2, 2), (2, 4, 2)]
+STREAM = [(S, sh) for S in range(9) for sh in SHAPES]
+
+
+@pytest.mark.parametrize("S,shape", STREAM, ids=[f"S{S}_k{k}_v{v}_st{st}" for S, (k, v, st) in STREAM])
+def test_stream_kernel(S, shape):
+    """Every num_blocks x stream shape (split, vectors per thread, ring
+    depth); T = 300 gives each persistent cluster several tokens, so every
+    stage and mailbox is reused with both parities."""
+    k, v, st = shape
+    i = S * 8 + SHAPES.index(shape)
+    d, o = bool(i & 1), bool(i & 2)
+    w = [-1, S, 8][i % 3]
+    wl = W.make_workload(300, S, capacity=9, has_delta=d, has_out_norm=o,
+                         block_write_idx=w, seed=i, mixing=True,
+                         slot_stride=7168 + 8 * (i % 2))
+    full_check(wl, tag=f"stream_S{S}_k{k}_v{v}_st{st}_d{int(d)}_o{int(o)}_w{w}",
+               kernel=ar.KERNEL_STREAM, split=k, vpt=v, stages=st)
+
+
+@pytest.mark.parametrize("T", [1, 2, 7, 1500])
+def test_stream_kernel_token_counts(T):
+    """Fewer tokens than clusters, and many tokens per cluster."""
+    wl = W.make_workload(T, 8, capacity=8, has_delta=True, has_out_norm=True,
+                         block_write_idx=3, seed=T, mixing=True)
+    full_check(wl, kernel=ar.KERNEL_STREAM)
+    full_check(wl, kernel=ar.KERNEL_STREAM, split=7, vpt=1, pdl=True)
+
+
+def test_split_kernel_at_prefill_size():
+    full_check(W.prefill(1024, 8, True, 7), kernel=ar.KERNEL_SPLIT)
+
+
+def test_zz_device_status_clean():
+    """No kernel recorded a stage-wait time-out during the tests above."""
+    assert ar.device_status() == 0
