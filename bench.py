@@ -181,6 +181,20 @@ def oracle_rate(wl, budget_s: float, threads: int):
     return n * passes / dt, n, passes, dt
 
 
+# ---- ranks --------------------------------------------------------------------
+
+def combine_ranks(dist, total_ms: float, tokens_per_rank: int, device=None):
+    """Whole-job throughput: the slowest rank's time, tokens summed over
+    ranks (each rank runs its own replica of the workload)."""
+    if dist is None:
+        return total_ms, tokens_per_rank / (total_ms / 1e3)
+    import torch
+    x = torch.tensor([total_ms], dtype=torch.float64, device=device)
+    dist.all_reduce(x, op=dist.ReduceOp.MAX)
+    tmax = float(x.item())
+    return tmax, tokens_per_rank * dist.get_world_size() / (tmax / 1e3)
+
+
 # ---- GPU arm ------------------------------------------------------------------
 
 def device_tensors(wl, torch, dev):
@@ -339,13 +353,7 @@ def run_ours(args, rank, world, local_rank, dist):
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
-    tmax = total_ms
-    if dist is not None:
-        x = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(x, op=dist.ReduceOp.MAX)
-        tmax = float(x.item())
-    tokens_total = wl.T * args.steps * world
-    value = tokens_total / (tmax / 1e3)
+    tmax, value = combine_ranks(dist, total_ms, wl.T * args.steps, dev)
     mean_launch_ms = statistics.mean(per)
     alg_bytes = wl.algorithmic_bytes()
     peak, peak_kind = measured_peaks()
@@ -381,10 +389,7 @@ def run_ours(args, rank, world, local_rank, dist):
         torch.cuda.empty_cache()
         e = e2e(ar, wl, torch, dev, stream, max(3, min(args.steps, args.e2e_steps)))
         if dist is not None:
-            x = torch.tensor([e["ms_per_step"]], dtype=torch.float64, device=dev)
-            dist.all_reduce(x, op=dist.ReduceOp.MAX)
-            e["ms_per_step"] = float(x.item())
-            e["value"] = wl.T * world / (e["ms_per_step"] / 1e3)
+            e["ms_per_step"], e["value"] = combine_ranks(dist, e["ms_per_step"], wl.T, dev)
         e["value"] = round(e["value"], 1)
         line["e2e"] = e
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
