@@ -36,8 +36,9 @@ struct Plan {
   int shape;   // index into the stream kernel's shape table
 };
 
-// Few tokens: one cluster per token, many small CTAs per token, so one
-// token's latency chain (load, reduce, exchange) runs on many SMs at once.
+// Few tokens: one cluster of 7 CTAs x 128 threads per token, all threads
+// active, so one token's latency chain (load, reduce, exchange) runs on 7 SMs
+// at once.
 // Many tokens: persistent clusters of 4 CTAs, 2 vectors per thread (112
 // threads per CTA) and a 2-deep TMA ring -- the fastest stream shape on
 // GB300 at 1024..8192 tokens.
@@ -50,7 +51,7 @@ attn_res_status_t make_plan(int64_t T, uint32_t flags, Plan* out) {
   pl.shape = -1;
   if (pl.kernel == 0) pl.kernel = T >= kStreamMinTokens ? ATTN_RES_KERNEL_STREAM : ATTN_RES_KERNEL_SPLIT;
   if (pl.kernel == ATTN_RES_KERNEL_SPLIT) {
-    if (pl.split == 0) pl.split = T <= 32 ? 8 : 7;
+    if (pl.split == 0) pl.split = 7;
     if (pl.vpt == 0) pl.vpt = 1;
     if (split_index(pl.split) < 0 || pl.stages != 0 || pl.vpt != 1) return ATTN_RES_EINVAL;
   } else if (pl.kernel == ATTN_RES_KERNEL_STREAM) {

@@ -116,14 +116,16 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
   return t;
 }
 // Wait for the phase of parity `parity` of an mbarrier of this CTA, at most
-// kWaitLimitNs.  Returns false on time-out.
+// about kWaitLimitNs.  Returns false on time-out.  The clock is read once at
+// the first miss and then every 1024 tries, so a waiting warp spends its
+// issue slots almost only on try_wait itself.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
-  while (!mbar_try_wait(bar, parity)) {
-    if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 1023u) == 0 && global_timer_ns() - t0 > kWaitLimitNs) return false;
   }
-  return true;
 }
 // Waits unless an earlier wait of this thread already failed; records the
 // failure once in the device status word.
@@ -174,16 +176,8 @@ __device__ __forceinline__ f32x2 f2_make(float lo, float hi) {
   asm("mov.b64 %0, {%1,%2};" : "=l"(r) : "f"(lo), "f"(hi));
   return r;
 }
-__device__ __forceinline__ float f2_lo(f32x2 a) {
-  float lo, hi;
-  asm("mov.b64 {%0,%1}, %2;" : "=f"(lo), "=f"(hi) : "l"(a));
-  return lo;
-}
-__device__ __forceinline__ float f2_hi(f32x2 a) {
-  float lo, hi;
-  asm("mov.b64 {%0,%1}, %2;" : "=f"(lo), "=f"(hi) : "l"(a));
-  return hi;
-}
+__device__ __forceinline__ float f2_lo(f32x2 a) { return __uint_as_float((uint32_t)a); }
+__device__ __forceinline__ float f2_hi(f32x2 a) { return __uint_as_float((uint32_t)(a >> 32)); }
 __device__ __forceinline__ f32x2 f2_fma(f32x2 a, f32x2 b, f32x2 c) {
   f32x2 d;
   asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));

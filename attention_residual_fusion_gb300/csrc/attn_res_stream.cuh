@@ -141,43 +141,48 @@ __global__ void __launch_bounds__(StreamCfg<S, HAS_DELTA, HAS_ONORM, K, VPT, STA
   make_query<VPT>(rw, qw, q);
   if (COMM) cluster_wait_acquire();
 
+  // Software pipeline over this cluster's tokens: B(j), refill, A(j+1), C(j)
+  // (phases in attn_res_token.cuh), so the exchanges of one token overlap the
+  // work of the next.  A peer runs at most one token ahead, which the
+  // double-buffered mailboxes allow.
   bool failed = false;
+  auto stage_of = [&](int64_t j) { return ring + (int)(j % STAGES) * ROWS * VPC + tid; };
+  auto phase_a = [&](int64_t j, uint4 (&cc)[VPT]) {
+    const int s = (int)(j % STAGES);
+    const int b = (int)(j & 1);
+    if (COMM && tid == 0) mailbox_expect<Tok>(mb, b, HAS_ONORM);
+    const bool was_failed = failed;
+    wait_or_flag(smem_addr(&full_bar[s]), (uint32_t)((j / STAGES) & 1), failed, p.err,
+                 kErrStageTimeout);
+    if (tid == 0 && !was_failed && !failed) pending &= ~(1u << s);
+    const uint4* stage = stage_of(j);
+    token_sums<S, HAS_DELTA, HAS_ONORM, K, NW, VPT>(
+        [&](int i, int v) { return active[v] ? stage[i * VPC + v * THREADS] : make_uint4(0, 0, 0, 0); },
+        q, mb, b, rank, warp, lane, cc);
+  };
+
+  uint4 c_cur[VPT];
+  if (ntok > 0) phase_a(0, c_cur);
   for (int64_t j = 0; j < ntok; ++j) {
     const int s = (int)(j % STAGES);
     const uint32_t sparity = (uint32_t)((j / STAGES) & 1);
     const int b = (int)(j & 1);                         // mailbox buffer
     const uint32_t bparity = (uint32_t)((j >> 1) & 1);  // its phase parity
     const int64_t t = cid + j * ncl;
-    if (COMM && tid == 0) mailbox_expect<Tok>(mb, b, HAS_ONORM);
+    const uint4* stage = stage_of(j);
 
-    const bool was_failed = failed;
-    wait_or_flag(smem_addr(&full_bar[s]), sparity, failed, p.err, kErrStageTimeout);
-    if (tid == 0 && !was_failed && !failed) pending &= ~(1u << s);
+    // B(j): softmax and mix; each warp releases the stage after its last read
+    f32x2 acc[VPT][4];
+    token_mix<S, HAS_DELTA, HAS_ONORM, K, NW, VPT>(
+        [&](int i, int v) { return active[v] ? stage[i * VPC + v * THREADS] : make_uint4(0, 0, 0, 0); },
+        mb, b, bparity, rank, warp, lane, p.eps, failed, p.err,
+        [&]() {
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_addr(&empty_bar[s]));
+        },
+        c_cur, acc);
 
-    const uint4* stage = ring + s * ROWS * VPC + tid;
-    auto row = [&](int i, int v) -> uint4 {
-      return active[v] ? stage[i * VPC + v * THREADS] : make_uint4(0, 0, 0, 0);
-    };
-    auto release = [&]() {
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_addr(&empty_bar[s]));
-    };
-    uint4 c[VPT], o[VPT];
-    mix_token<S, HAS_DELTA, HAS_ONORM, K, NW, VPT>(row, q, ow, mb, b, bparity, rank, warp, lane,
-                                                    p.eps, p.out_eps, failed, p.err, release, c, o);
-#pragma unroll
-    for (int v = 0; v < VPT; ++v) {
-      if (active[v]) {
-        const int64_t col = slice0 + (int64_t)(tid + v * THREADS) * kVec;
-        st_row(p.out + t * p.out_row + col, o[v]);
-        if (HAS_DELTA) st_row(p.prefix + t * p.prefix_row + col, c[v]);
-        if (p.write_idx >= 0)
-          st_row(p.blocks + t * p.blocks_token + (int64_t)p.write_idx * p.blocks_slot + col, c[v]);
-      }
-    }
-
-    // refill stage s with the token STAGES ahead, once every local warp is
-    // done with it
+    // refill stage s with the token STAGES ahead once every local warp is done
     if (tid == 0 && !failed && j + STAGES < ntok) {
       wait_or_flag(smem_addr(&empty_bar[s]), sparity, failed, p.err, kErrStageTimeout);
       if (!failed) {
@@ -188,6 +193,27 @@ __global__ void __launch_bounds__(StreamCfg<S, HAS_DELTA, HAS_ONORM, K, VPT, STA
         pending |= 1u << s;
         pending_parity = (pending_parity & ~(1u << s)) | ((sparity ^ 1u) << s);
       }
+    }
+
+    // A(j+1): next token's partial sums go out while this token's norm
+    // exchange is in flight
+    uint4 c_next[VPT];
+    if (j + 1 < ntok) phase_a(j + 1, c_next);
+
+    // C(j): output norm and stores
+    uint4 o[VPT];
+    token_finish<S, HAS_DELTA, HAS_ONORM, K, NW, VPT>(mb, b, bparity, lane, p.out_eps, failed,
+                                                       p.err, ow, acc, o);
+#pragma unroll
+    for (int v = 0; v < VPT; ++v) {
+      if (active[v]) {
+        const int64_t col = slice0 + (int64_t)(tid + v * THREADS) * kVec;
+        st_row(p.out + t * p.out_row + col, o[v]);
+        if (HAS_DELTA) st_row(p.prefix + t * p.prefix_row + col, c_cur[v]);
+        if (p.write_idx >= 0)
+          st_row(p.blocks + t * p.blocks_token + (int64_t)p.write_idx * p.blocks_slot + col, c_cur[v]);
+      }
+      c_cur[v] = c_next[v];
     }
   }
 

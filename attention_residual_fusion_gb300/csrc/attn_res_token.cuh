@@ -76,25 +76,25 @@ __device__ __forceinline__ void make_query(const uint4 (&rw)[VPT], const uint4 (
       q[v][k] = f2_mul(bf2_widen(vword(rw[v], k)), bf2_widen(vword(qw[v], k)));
 }
 
-// row(i, v): vector v of row i (bank rows 0..S-1, prefix S, delta S+1);
-// zeros for idle threads.  after_mix(): called once the thread no longer
-// needs any row data of this token.  b / parity: mailbox buffer and its phase
-// parity for this token.  Writes c (current-layer row) and out.
-template <int S, bool HAS_DELTA, bool HAS_ONORM, int K, int NW, int VPT, class Row,
-          class AfterMix>
-__device__ __forceinline__ void mix_token(Row row, const f32x2 (&q)[VPT][4],
-                                          const uint4 (&ow)[VPT],
-                                          typename TokenCfg<S, HAS_DELTA, HAS_ONORM, K, NW>::Box& mb,
-                                          int b, uint32_t parity, uint32_t rank, int warp,
-                                          int lane, float eps, float out_eps, bool& failed,
-                                          unsigned* err, AfterMix after_mix, uint4 (&c)[VPT],
-                                          uint4 (&out)[VPT]) {
+// The token runs in three phases so that a persistent kernel can overlap one
+// token's exchanges with the next token's work:
+//   A  token_sums:   current-layer row c, partial sums, send them to every CTA
+//   B  token_mix:    wait for all sums, softmax, mix, release the row data,
+//                    send sum(acc^2) (output norm)
+//   C  token_finish: wait for all sum(acc^2), scale, pack the output
+// row(i, v): vector v of row i (bank rows 0..S-1, prefix S, delta S+1),
+// zeros for idle threads.  b / parity: mailbox buffer of this token and its
+// phase parity.
+
+template <int S, bool HAS_DELTA, bool HAS_ONORM, int K, int NW, int VPT, class Row>
+__device__ __forceinline__ void token_sums(Row row, const f32x2 (&q)[VPT][4],
+                                           typename TokenCfg<S, HAS_DELTA, HAS_ONORM, K, NW>::Box& mb,
+                                           int b, uint32_t rank, int warp, int lane,
+                                           uint4 (&c)[VPT]) {
   using C = TokenCfg<S, HAS_DELTA, HAS_ONORM, K, NW>;
   constexpr int N = C::N;
   constexpr int NR = C::NR;
   constexpr int P = C::P;
-  const int src = (int)rank * NW + warp;  // this warp's slot in every mailbox
-
 #pragma unroll
   for (int v = 0; v < VPT; ++v) {
     if constexpr (HAS_DELTA) {
@@ -103,15 +103,7 @@ __device__ __forceinline__ void mix_token(Row row, const f32x2 (&q)[VPT][4],
       c[v] = row(S, v);
     }
   }
-
-  f32x2 acc[VPT][4];
-  if constexpr (S == 0) {
-#pragma unroll
-    for (int v = 0; v < VPT; ++v)
-#pragma unroll
-      for (int k = 0; k < 4; ++k) acc[v][k] = bf2_widen(vword(c[v], k));
-    after_mix();
-  } else {
+  if constexpr (S > 0) {
     // per-source partial sums over this thread's columns
     float part[P];
 #pragma unroll
@@ -136,11 +128,34 @@ __device__ __forceinline__ void mix_token(Row row, const f32x2 (&q)[VPT][4],
     const float tv = reduce_scatter<P>(part, lane);
     const int idx = lane >> C::SHIFT;
     if ((lane & ((1 << C::SHIFT) - 1)) == 0 && idx < NR) {
+      const int src = (int)rank * NW + warp;
       const uint32_t a = smem_addr(&mb.sums[b][src][idx]);
       const uint32_t bar = smem_addr(&mb.bar_sums[b]);
 #pragma unroll
       for (int r = 0; r < K; ++r) st_async_f32(map_rank(a, r), tv, map_rank(bar, r));
     }
+  }
+}
+
+// after_mix(): called once the thread no longer needs any row data.
+template <int S, bool HAS_DELTA, bool HAS_ONORM, int K, int NW, int VPT, class Row,
+          class AfterMix>
+__device__ __forceinline__ void token_mix(Row row,
+                                          typename TokenCfg<S, HAS_DELTA, HAS_ONORM, K, NW>::Box& mb,
+                                          int b, uint32_t parity, uint32_t rank, int warp,
+                                          int lane, float eps, bool& failed, unsigned* err,
+                                          AfterMix after_mix, const uint4 (&c)[VPT],
+                                          f32x2 (&acc)[VPT][4]) {
+  using C = TokenCfg<S, HAS_DELTA, HAS_ONORM, K, NW>;
+  constexpr int N = C::N;
+  constexpr int NR = C::NR;
+  if constexpr (S == 0) {
+#pragma unroll
+    for (int v = 0; v < VPT; ++v)
+#pragma unroll
+      for (int k = 0; k < 4; ++k) acc[v][k] = bf2_widen(vword(c[v], k));
+    after_mix();
+  } else {
     wait_or_flag(smem_addr(&mb.bar_sums[b]), parity, failed, err, kErrExchangeTimeout);
     // token totals in a fixed order, logits and softmax (every warp)
     float tot = 0.f;
@@ -172,7 +187,6 @@ __device__ __forceinline__ void mix_token(Row row, const f32x2 (&q)[VPT][4],
     }
     after_mix();
   }
-
   if constexpr (HAS_ONORM) {
     f32x2 sq2 = 0ull;
 #pragma unroll
@@ -181,8 +195,17 @@ __device__ __forceinline__ void mix_token(Row row, const f32x2 (&q)[VPT][4],
       for (int k = 0; k < 4; ++k) sq2 = f2_fma(acc[v][k], acc[v][k], sq2);
     const float sq = warp_sum(f2_lo(sq2) + f2_hi(sq2));
     if (lane < K)
-      st_async_f32(map_rank(smem_addr(&mb.sq[b][src]), lane), sq,
+      st_async_f32(map_rank(smem_addr(&mb.sq[b][(int)rank * NW + warp]), lane), sq,
                    map_rank(smem_addr(&mb.bar_sq[b]), lane));
+  }
+}
+
+template <int S, bool HAS_DELTA, bool HAS_ONORM, int K, int NW, int VPT>
+__device__ __forceinline__ void token_finish(typename TokenCfg<S, HAS_DELTA, HAS_ONORM, K, NW>::Box& mb,
+                                             int b, uint32_t parity, int lane, float out_eps,
+                                             bool& failed, unsigned* err, const uint4 (&ow)[VPT],
+                                             f32x2 (&acc)[VPT][4], uint4 (&out)[VPT]) {
+  if constexpr (HAS_ONORM) {
     wait_or_flag(smem_addr(&mb.bar_sq[b]), parity, failed, err, kErrExchangeTimeout);
     const float tot = warp_sum(lane < K * NW ? mb.sq[b][lane] : 0.f);
     const float ro = 1.0f / sqrtf(tot / (float)kH + out_eps);
@@ -198,6 +221,24 @@ __device__ __forceinline__ void mix_token(Row row, const f32x2 (&q)[VPT][4],
                         pack_bf16x2(f2_lo(acc[v][1]), f2_hi(acc[v][1])),
                         pack_bf16x2(f2_lo(acc[v][2]), f2_hi(acc[v][2])),
                         pack_bf16x2(f2_lo(acc[v][3]), f2_hi(acc[v][3])));
+}
+
+// The three phases back to back (one token, no overlap).
+template <int S, bool HAS_DELTA, bool HAS_ONORM, int K, int NW, int VPT, class Row,
+          class AfterMix>
+__device__ __forceinline__ void mix_token(Row row, const f32x2 (&q)[VPT][4],
+                                          const uint4 (&ow)[VPT],
+                                          typename TokenCfg<S, HAS_DELTA, HAS_ONORM, K, NW>::Box& mb,
+                                          int b, uint32_t parity, uint32_t rank, int warp,
+                                          int lane, float eps, float out_eps, bool& failed,
+                                          unsigned* err, AfterMix after_mix, uint4 (&c)[VPT],
+                                          uint4 (&out)[VPT]) {
+  f32x2 acc[VPT][4];
+  token_sums<S, HAS_DELTA, HAS_ONORM, K, NW, VPT>(row, q, mb, b, rank, warp, lane, c);
+  token_mix<S, HAS_DELTA, HAS_ONORM, K, NW, VPT>(row, mb, b, parity, rank, warp, lane, eps, failed,
+                                                 err, after_mix, c, acc);
+  token_finish<S, HAS_DELTA, HAS_ONORM, K, NW, VPT>(mb, b, parity, lane, out_eps, failed, err, ow,
+                                                    acc, out);
 }
 
 }  // namespace attn_res_dev

@@ -50,6 +50,9 @@ def make(name: str):
     from attention_residual_fusion_gb300 import workloads as W
     if name == "long_prefill":
         return W.long_prefill(), "long prefill T=8192, S=8, bank [8192,9,7232] padded, delta, output norm, write-back slot 8, per-block scales U(1,30)"
+    if name.startswith("long_prefill:"):   # same layout, fewer tokens (profiling)
+        T = int(name.split(":")[1])
+        return W.long_prefill(T), f"long prefill layout at T={T}, S=8, bank [T,9,7232] padded, delta, output norm, write-back slot 8"
     if name == "single_token":
         return W.single_token(), "single token T=1, S=4, bank [1,8,7168], delta, output norm, no write-back"
     kind, *a = name.split(":")
@@ -101,34 +104,43 @@ def recorded_traffic(workload: str):
 # ---- clocks -------------------------------------------------------------------
 
 class ClockSampler:
-    """nvidia-smi samples of SM clock and throttle reasons while running."""
-    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi samples (every 20 ms) of SM clock and throttle reasons.
+    `mark()` brackets the timed region; the summary uses the samples taken
+    inside it, or the two nearest ones when the region is shorter than the
+    sampling period."""
+    Q = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
         self.proc = None
-        self.lines = []
+        self.samples = []  # (host time, fields)
+        self.window = None
 
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "20"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
+            time.sleep(0.3)  # let nvidia-smi start sampling
         except Exception:
             self.proc = None
         return self
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.samples.append((time.time(), [x.strip() for x in line.split(",")]))
+
+    def mark(self, t0: float, t1: float):
+        self.window = (t0, t1)
 
     def __exit__(self, *exc):
         if self.proc is not None:
+            time.sleep(0.05)
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
@@ -139,23 +151,26 @@ class ClockSampler:
     def summary(self):
         if self.proc is None:
             return None
+        good = [(t, f) for t, f in self.samples if len(f) >= 10]
+        if self.window is not None and good:
+            t0, t1 = self.window
+            inside = [(t, f) for t, f in good if t0 <= t <= t1]
+            if not inside:
+                mid = (t0 + t1) / 2
+                inside = sorted(good, key=lambda s: abs(s[0] - mid))[:2]
+            good = inside
         sm, mx, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
-            f = [x.strip() for x in ln.split(",")]
-            if len(f) < 9:
-                continue
+        for _, f in good:
             try:
-                sm.append(float(f[1]))
-                mx = float(f[2])
+                sm.append(float(f[2]))
+                mx = float(f[3])
             except ValueError:
                 continue
-            for n, v in zip(names, f[5:9]):
+            for n, v in zip(names, f[6:10]):
                 if v.lower() == "active":
                     reasons.add(n)
-        if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": 0}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx,
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
@@ -349,7 +364,9 @@ def run_ours(args, rank, world, local_rank, dist):
         dist.barrier()
     torch.cuda.synchronize()
     with ClockSampler(local_rank) as clk:
+        w0 = time.time()
         total_ms, per = time_device(ar, wl, t, torch, stream, args.steps, 0)
+        clk.mark(w0, time.time())
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()

@@ -43,7 +43,7 @@ def test_constants(lib):
 
 def test_launch_shape(lib):
     ls = ar.launch_shape
-    assert ls(1, 4, True) == dict(kernel="split", split=8, stages=0, threads=128, ctas=8, cluster=8)
+    assert ls(1, 4, True) == dict(kernel="split", split=7, stages=0, threads=128, ctas=7, cluster=7)
     assert ls(64, 8, False) == dict(kernel="split", split=7, stages=0, threads=128, ctas=448, cluster=7)
     assert ls(8192, 8, True) == dict(kernel="stream", split=4, stages=2, threads=128, ctas=0, cluster=4)
     # no softmax and no output norm: the CTAs of a token never talk
