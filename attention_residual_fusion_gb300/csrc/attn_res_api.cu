@@ -39,9 +39,9 @@ struct Plan {
 // Few tokens: one cluster of 7 CTAs x 128 threads per token, all threads
 // active, so one token's latency chain (load, reduce, exchange) runs on 7 SMs
 // at once.
-// Many tokens: persistent clusters of 4 CTAs, 2 vectors per thread (112
-// threads per CTA) and a 2-deep TMA ring -- the fastest stream shape on
-// GB300 at 1024..8192 tokens.
+// Many tokens: persistent clusters of 7 CTAs, 2 vectors per thread (64
+// threads per CTA, 6 CTAs per SM) and a 2-deep TMA ring -- the fastest
+// stream shape on GB300 from 256 to 8192 tokens.
 attn_res_status_t make_plan(int64_t T, uint32_t flags, Plan* out) {
   Plan pl;
   pl.kernel = static_cast<int>((flags >> 16) & 0xfu);
@@ -55,7 +55,7 @@ attn_res_status_t make_plan(int64_t T, uint32_t flags, Plan* out) {
     if (pl.vpt == 0) pl.vpt = 1;
     if (split_index(pl.split) < 0 || pl.stages != 0 || pl.vpt != 1) return ATTN_RES_EINVAL;
   } else if (pl.kernel == ATTN_RES_KERNEL_STREAM) {
-    if (pl.split == 0) pl.split = 4;
+    if (pl.split == 0) pl.split = 7;
     if (pl.stages == 0) pl.stages = 2;
     if (pl.vpt == 0) pl.vpt = 2;
     pl.shape = stream_shape_index(pl.split, pl.vpt, pl.stages);

@@ -117,8 +117,7 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
 }
 // Wait for the phase of parity `parity` of an mbarrier of this CTA, at most
 // about kWaitLimitNs.  Returns false on time-out.  The clock is read once at
-// the first miss and then every 1024 tries, so a waiting warp spends its
-// issue slots almost only on try_wait itself.
+// the first miss and then every 1024 tries.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
@@ -205,11 +204,13 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   memcpy(&u, &h, sizeof u);
   return u;
 }
-// fp32 add of two bf16 values, then round to nearest even: equal to the
-// correctly rounded bf16 sum (24 >= 2*8+2 bits, so the double rounding is
-// innocuous).
+// Packed bf16 add, round to nearest even: the correctly rounded bf16 sum of
+// each pair (the same value as an fp32 add followed by RNE to bf16, since
+// 24 >= 2*8+2 bits makes that double rounding innocuous).
 __device__ __forceinline__ uint32_t add_bf16x2(uint32_t a, uint32_t b) {
-  return pack_bf16x2(bf_lo(a) + bf_lo(b), bf_hi(a) + bf_hi(b));
+  uint32_t d;
+  asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
 }
 __device__ __forceinline__ uint4 add_bf16x8(const uint4& a, const uint4& b) {
   return make_uint4(add_bf16x2(a.x, b.x), add_bf16x2(a.y, b.y), add_bf16x2(a.z, b.z),

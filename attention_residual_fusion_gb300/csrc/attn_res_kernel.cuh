@@ -99,6 +99,10 @@ __global__ void __launch_bounds__(SplitCfg<S, HAS_DELTA, HAS_ONORM, K>::THREADS)
 
   bool failed = false;
   uint4 c[1], o[1];
+  {
+    const uint4 pre[1] = {x[S]}, del[1] = {x[ROWS - 1]};
+    current_row<HAS_DELTA, 1>(pre, del, c);
+  }
   mix_token<S, HAS_DELTA, HAS_ONORM, K, C::NW, 1>(
       [&](int i, int) { return x[i]; }, q, owv, mb, 0, 0u, rank, warp, lane, p.eps, p.out_eps,
       failed, p.err, [] {}, c, o);

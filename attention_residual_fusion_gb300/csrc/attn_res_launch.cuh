@@ -71,8 +71,8 @@ cudaError_t launch_split(const Params& p, int64_t T, bool pdl,
 struct StreamShape {
   int k, vpt, stages;
 };
-constexpr StreamShape kStreamShapes[] = {{7, 1, 2}, {7, 2, 2}, {7, 4, 2}, {4, 2, 2},
-                                         {4, 4, 2}, {4, 2, 3}, {14, 2, 2}, {2, 4, 2}};
+constexpr StreamShape kStreamShapes[] = {{7, 1, 2}, {7, 2, 2}, {7, 2, 3}, {7, 4, 2},
+                                         {4, 2, 2}, {4, 2, 3}, {14, 1, 2}, {14, 2, 2}};
 constexpr int kNumStreamShapes = sizeof(kStreamShapes) / sizeof(kStreamShapes[0]);
 
 inline int stream_shape_index(int k, int vpt, int stages) {

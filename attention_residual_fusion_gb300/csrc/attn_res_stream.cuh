@@ -3,26 +3,32 @@
 // Same column split and per-token arithmetic as the split kernel (one cluster
 // of K CTAs per token row, CTA r owning a contiguous 1/K of every row, see
 // attn_res_token.cuh), but each cluster loops over many tokens and keeps the
-// HBM stream going while it reduces:
+// HBM stream going while it computes:
 //
 //   * thread 0 of each CTA issues bulk copies (cp.async.bulk, the TMA
-//     engine's one-dimensional form) of the CTA's slice of every source row of
-//     a token into one stage of a STAGES-deep shared-memory ring; the copies
-//     complete on the stage's `full` mbarrier (expect-tx of the stage's bytes);
+//     engine's one-dimensional form) of the CTA's slice of the token's bank
+//     rows into one stage of a STAGES-deep shared-memory ring; the copies
+//     complete on the stage's `full` mbarrier (expect-tx of the stage bytes);
+//   * each thread loads its vectors of the token's prefix and delta rows
+//     straight into registers one token ahead, so the ring holds bank rows
+//     only -- shared memory, not registers, is what limits how many CTAs
+//     (and so how many tokens) an SM keeps in flight;
 //   * every thread waits on `full` (bounded: on time-out the kernel records an
-//     error bit, stops issuing copies and runs to completion) and reads its VPT
-//     vectors of every row straight from the stage, once for the partial sums
-//     and once for the mix -- rows are not copied into registers, which keeps
-//     the register footprint per token small and lets more clusters run;
+//     error bit, stops issuing copies and runs to completion) and reads its
+//     vectors straight from the stage, once for the partial sums and once for
+//     the mix;
 //   * after its last read of the stage each warp arrives on the stage's
 //     `empty` mbarrier; thread 0 waits on it, fences the generic-proxy reads
-//     against the async proxy, and refills the stage with the token STAGES
-//     ahead.
+//     against the async proxy and refills the stage with the token STAGES
+//     ahead;
+//   * the token phases run software-pipelined: B(j) (softmax, mix), refill,
+//     A(j+1) (partial sums of the next token), C(j) (output norm, stores), so
+//     one token's exchanges overlap the next token's work.
 //
 // Staging rows in shared memory with TMA and mbarriers follows the design of
 // the kernel excerpted in the prhub summaries of vllm PR #54261 and #50185;
-// the pages chunk sources with an online softmax, here a stage holds all
-// sources of one token slice and the softmax is taken once.
+// the pages chunk sources with an online softmax, here a stage holds all bank
+// rows of one token slice and the softmax is taken once.
 #pragma once
 
 #include "attn_res_token.cuh"
@@ -31,14 +37,13 @@ namespace attn_res_dev {
 
 template <int S, bool HAS_DELTA, bool HAS_ONORM, int K, int VPT, int STAGES>
 struct StreamCfg {
-  static constexpr int VPC = kNV / K;                      // vectors per CTA per row
+  static constexpr int VPC = kNV / K;  // vectors per CTA per row
   static constexpr int THREADS = (VPC / VPT + 31) / 32 * 32;
   static constexpr int NW = THREADS / 32;
   using Tok = TokenCfg<S, HAS_DELTA, HAS_ONORM, K, NW>;
-  static constexpr int ROWS = Tok::ROWS;  // bank rows, prefix, delta
   static constexpr bool COMM = Tok::COMM;
   static constexpr uint32_t SLICE_BYTES = VPC * 16;  // one row's slice, multiple of 16
-  static constexpr uint32_t STAGE_BYTES = ROWS * SLICE_BYTES;
+  static constexpr uint32_t STAGE_BYTES = S * SLICE_BYTES;
   static constexpr uint32_t SMEM_BYTES = STAGES * STAGE_BYTES;
   static_assert(kNV % K == 0, "split must divide the 896 row vectors");
   static_assert(VPC % VPT == 0, "vectors per thread must divide the slice");
@@ -50,13 +55,12 @@ __global__ void __launch_bounds__(StreamCfg<S, HAS_DELTA, HAS_ONORM, K, VPT, STA
     attn_res_stream_kernel(const Params p, const int64_t T) {
   using C = StreamCfg<S, HAS_DELTA, HAS_ONORM, K, VPT, STAGES>;
   using Tok = typename C::Tok;
-  constexpr int ROWS = C::ROWS;
   constexpr int VPC = C::VPC;
   constexpr int THREADS = C::THREADS;
   constexpr int NW = C::NW;
   constexpr bool COMM = C::COMM;
 
-  extern __shared__ __align__(128) uint4 ring[];  // [STAGES][ROWS][VPC]
+  extern __shared__ __align__(128) uint4 ring[];  // [STAGES][S][VPC]
   __shared__ __align__(8) unsigned long long full_bar[STAGES];
   __shared__ __align__(8) unsigned long long empty_bar[STAGES];
   __shared__ typename Tok::Box mb;
@@ -72,8 +76,12 @@ __global__ void __launch_bounds__(StreamCfg<S, HAS_DELTA, HAS_ONORM, K, VPT, STA
   const uint32_t ring_addr = smem_addr(ring);
   // vector v of this thread: index tid + v * THREADS within the CTA's slice
   bool active[VPT];
+  int64_t col[VPT];
 #pragma unroll
-  for (int v = 0; v < VPT; ++v) active[v] = tid + v * THREADS < VPC;
+  for (int v = 0; v < VPT; ++v) {
+    active[v] = ((v + 1) * THREADS <= VPC) || (tid + v * THREADS < VPC);
+    col[v] = slice0 + (int64_t)(tid + v * THREADS) * kVec;
+  }
 
   if (tid == 0) {
 #pragma unroll
@@ -90,31 +98,38 @@ __global__ void __launch_bounds__(StreamCfg<S, HAS_DELTA, HAS_ONORM, K, VPT, STA
     __syncthreads();
   }
 
-  // producer side (thread 0): copies of one token into one stage
-  auto stage_dst = [&](int s, int row) -> uint32_t {
-    return ring_addr + (uint32_t)(s * ROWS + row) * C::SLICE_BYTES;
-  };
+  // producer side (thread 0): the bank rows of one token into one stage
   auto issue_bank = [&](int64_t t, int s) {
     const uint32_t bar = smem_addr(&full_bar[s]);
     mbar_arrive_expect_tx(bar, C::STAGE_BYTES);
     const uint16_t* bp = p.blocks + t * p.blocks_token + slice0;
 #pragma unroll
     for (int i = 0; i < S; ++i)
-      bulk_load(stage_dst(s, i), bp + (int64_t)i * p.blocks_slot, C::SLICE_BYTES, bar);
+      bulk_load(ring_addr + (uint32_t)(s * S + i) * C::SLICE_BYTES, bp + (int64_t)i * p.blocks_slot,
+                C::SLICE_BYTES, bar);
   };
-  auto issue_current = [&](int64_t t, int s) {
-    const uint32_t bar = smem_addr(&full_bar[s]);
-    bulk_load(stage_dst(s, S), p.prefix + t * p.prefix_row + slice0, C::SLICE_BYTES, bar);
-    if (HAS_DELTA)
-      bulk_load(stage_dst(s, S + 1), p.delta + t * p.delta_row + slice0, C::SLICE_BYTES, bar);
+  // every thread: its vectors of the token's prefix and delta rows
+  auto load_current = [&](int64_t t, uint4 (&pre)[VPT], uint4 (&del)[VPT]) {
+#pragma unroll
+    for (int v = 0; v < VPT; ++v) {
+      pre[v] = del[v] = make_uint4(0, 0, 0, 0);
+      if (active[v]) {
+        pre[v] = ld_row(p.prefix + t * p.prefix_row + col[v]);
+        if (HAS_DELTA) del[v] = ld_row(p.delta + t * p.delta_row + col[v]);
+      }
+    }
   };
 
   // prologue: bank rows of the first STAGES tokens before the grid-dependency
-  // wait, prefix and delta after it.  Thread 0 also tracks the stages whose
-  // last issued copies it has not yet seen complete, and that issue's parity.
+  // wait; prefix and delta (produced upstream) after it.  Thread 0 also
+  // tracks the stages whose last issued copies it has not yet seen complete,
+  // and that issue's parity.
   uint32_t pending = 0, pending_parity = 0;
   if (tid == 0) {
-    for (int s = 0; s < STAGES && s < ntok; ++s) issue_bank(cid + s * ncl, s);
+    for (int s = 0; s < STAGES && s < ntok; ++s) {
+      issue_bank(cid + s * ncl, s);
+      pending |= 1u << s;  // first use of every stage: parity 0
+    }
   }
   // weights: read-only, independent of the preceding kernel
   uint4 rw[VPT], qw[VPT], ow[VPT];
@@ -122,19 +137,14 @@ __global__ void __launch_bounds__(StreamCfg<S, HAS_DELTA, HAS_ONORM, K, VPT, STA
   for (int v = 0; v < VPT; ++v) {
     rw[v] = qw[v] = ow[v] = make_uint4(0, 0, 0, 0);
     if (active[v]) {
-      const int64_t col = slice0 + (int64_t)(tid + v * THREADS) * kVec;
-      rw[v] = ld_weight(p.rms_w + col);
-      qw[v] = ld_weight(p.res_w + col);
-      if (HAS_ONORM) ow[v] = ld_weight(p.onw + col);
+      rw[v] = ld_weight(p.rms_w + col[v]);
+      qw[v] = ld_weight(p.res_w + col[v]);
+      if (HAS_ONORM) ow[v] = ld_weight(p.onw + col[v]);
     }
   }
   grid_dep_wait();  // every thread: also orders our stores after the producer's work
-  if (tid == 0) {
-    for (int s = 0; s < STAGES && s < ntok; ++s) {
-      issue_current(cid + s * ncl, s);
-      pending |= 1u << s;  // first use of every stage: parity 0
-    }
-  }
+  uint4 pre[VPT], del[VPT];  // prefix and delta of the next token to start
+  if (ntok > 0) load_current(cid, pre, del);
   grid_dep_launch_dependents();
 
   f32x2 q[VPT][4];
@@ -142,15 +152,18 @@ __global__ void __launch_bounds__(StreamCfg<S, HAS_DELTA, HAS_ONORM, K, VPT, STA
   if (COMM) cluster_wait_acquire();
 
   // Software pipeline over this cluster's tokens: B(j), refill, A(j+1), C(j)
-  // (phases in attn_res_token.cuh), so the exchanges of one token overlap the
-  // work of the next.  A peer runs at most one token ahead, which the
-  // double-buffered mailboxes allow.
+  // (phases in attn_res_token.cuh).  A peer runs at most one token ahead,
+  // which the double-buffered mailboxes allow.
   bool failed = false;
-  auto stage_of = [&](int64_t j) { return ring + (int)(j % STAGES) * ROWS * VPC + tid; };
+  auto stage_of = [&](int64_t j) { return ring + (int)(j % STAGES) * S * VPC + tid; };
+  // A(j): current row; then, its prefix/delta registers free, the next
+  // token's prefix/delta loads go out; then the partial sums.
   auto phase_a = [&](int64_t j, uint4 (&cc)[VPT]) {
     const int s = (int)(j % STAGES);
     const int b = (int)(j & 1);
     if (COMM && tid == 0) mailbox_expect<Tok>(mb, b, HAS_ONORM);
+    current_row<HAS_DELTA, VPT>(pre, del, cc);
+    if (j + 1 < ntok) load_current(cid + (j + 1) * ncl, pre, del);
     const bool was_failed = failed;
     wait_or_flag(smem_addr(&full_bar[s]), (uint32_t)((j / STAGES) & 1), failed, p.err,
                  kErrStageTimeout);
@@ -158,7 +171,7 @@ __global__ void __launch_bounds__(StreamCfg<S, HAS_DELTA, HAS_ONORM, K, VPT, STA
     const uint4* stage = stage_of(j);
     token_sums<S, HAS_DELTA, HAS_ONORM, K, NW, VPT>(
         [&](int i, int v) { return active[v] ? stage[i * VPC + v * THREADS] : make_uint4(0, 0, 0, 0); },
-        q, mb, b, rank, warp, lane, cc);
+        cc, q, mb, b, rank, warp, lane);
   };
 
   uint4 c_cur[VPT];
@@ -187,9 +200,7 @@ __global__ void __launch_bounds__(StreamCfg<S, HAS_DELTA, HAS_ONORM, K, VPT, STA
       wait_or_flag(smem_addr(&empty_bar[s]), sparity, failed, p.err, kErrStageTimeout);
       if (!failed) {
         fence_proxy_async_smem();
-        const int64_t tn = cid + (j + STAGES) * ncl;
-        issue_bank(tn, s);
-        issue_current(tn, s);
+        issue_bank(cid + (j + STAGES) * ncl, s);
         pending |= 1u << s;
         pending_parity = (pending_parity & ~(1u << s)) | ((sparity ^ 1u) << s);
       }
@@ -207,11 +218,11 @@ __global__ void __launch_bounds__(StreamCfg<S, HAS_DELTA, HAS_ONORM, K, VPT, STA
 #pragma unroll
     for (int v = 0; v < VPT; ++v) {
       if (active[v]) {
-        const int64_t col = slice0 + (int64_t)(tid + v * THREADS) * kVec;
-        st_row(p.out + t * p.out_row + col, o[v]);
-        if (HAS_DELTA) st_row(p.prefix + t * p.prefix_row + col, c_cur[v]);
+        st_row(p.out + t * p.out_row + col[v], o[v]);
+        if (HAS_DELTA) st_row(p.prefix + t * p.prefix_row + col[v], c_cur[v]);
         if (p.write_idx >= 0)
-          st_row(p.blocks + t * p.blocks_token + (int64_t)p.write_idx * p.blocks_slot + col, c_cur[v]);
+          st_row(p.blocks + t * p.blocks_token + (int64_t)p.write_idx * p.blocks_slot + col[v],
+                 c_cur[v]);
       }
       c_cur[v] = c_next[v];
     }

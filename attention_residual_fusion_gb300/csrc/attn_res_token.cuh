@@ -82,27 +82,28 @@ __device__ __forceinline__ void make_query(const uint4 (&rw)[VPT], const uint4 (
 //   B  token_mix:    wait for all sums, softmax, mix, release the row data,
 //                    send sum(acc^2) (output norm)
 //   C  token_finish: wait for all sum(acc^2), scale, pack the output
-// row(i, v): vector v of row i (bank rows 0..S-1, prefix S, delta S+1),
-// zeros for idle threads.  b / parity: mailbox buffer of this token and its
-// phase parity.
+// Rows are zeros for idle threads.  b / parity: mailbox buffer of this token
+// and its phase parity.
 
+// Current-layer row from this thread's prefix and delta vectors.
+template <bool HAS_DELTA, int VPT>
+__device__ __forceinline__ void current_row(const uint4 (&pre)[VPT], const uint4 (&del)[VPT],
+                                            uint4 (&c)[VPT]) {
+#pragma unroll
+  for (int v = 0; v < VPT; ++v) c[v] = HAS_DELTA ? add_bf16x8(pre[v], del[v]) : pre[v];
+}
+
+// row(i, v): vector v of bank row i < S; c: the current-layer row (the last
+// source).
 template <int S, bool HAS_DELTA, bool HAS_ONORM, int K, int NW, int VPT, class Row>
-__device__ __forceinline__ void token_sums(Row row, const f32x2 (&q)[VPT][4],
+__device__ __forceinline__ void token_sums(Row row, const uint4 (&c)[VPT],
+                                           const f32x2 (&q)[VPT][4],
                                            typename TokenCfg<S, HAS_DELTA, HAS_ONORM, K, NW>::Box& mb,
-                                           int b, uint32_t rank, int warp, int lane,
-                                           uint4 (&c)[VPT]) {
+                                           int b, uint32_t rank, int warp, int lane) {
   using C = TokenCfg<S, HAS_DELTA, HAS_ONORM, K, NW>;
   constexpr int N = C::N;
   constexpr int NR = C::NR;
   constexpr int P = C::P;
-#pragma unroll
-  for (int v = 0; v < VPT; ++v) {
-    if constexpr (HAS_DELTA) {
-      c[v] = add_bf16x8(row(S, v), row(S + 1, v));
-    } else {
-      c[v] = row(S, v);
-    }
-  }
   if constexpr (S > 0) {
     // per-source partial sums over this thread's columns
     float part[P];
@@ -223,7 +224,8 @@ __device__ __forceinline__ void token_finish(typename TokenCfg<S, HAS_DELTA, HAS
                         pack_bf16x2(f2_lo(acc[v][3]), f2_hi(acc[v][3])));
 }
 
-// The three phases back to back (one token, no overlap).
+// The three phases back to back (one token, no overlap); c must hold the
+// current-layer row.
 template <int S, bool HAS_DELTA, bool HAS_ONORM, int K, int NW, int VPT, class Row,
           class AfterMix>
 __device__ __forceinline__ void mix_token(Row row, const f32x2 (&q)[VPT][4],
@@ -231,10 +233,10 @@ __device__ __forceinline__ void mix_token(Row row, const f32x2 (&q)[VPT][4],
                                           typename TokenCfg<S, HAS_DELTA, HAS_ONORM, K, NW>::Box& mb,
                                           int b, uint32_t parity, uint32_t rank, int warp,
                                           int lane, float eps, float out_eps, bool& failed,
-                                          unsigned* err, AfterMix after_mix, uint4 (&c)[VPT],
+                                          unsigned* err, AfterMix after_mix, const uint4 (&c)[VPT],
                                           uint4 (&out)[VPT]) {
   f32x2 acc[VPT][4];
-  token_sums<S, HAS_DELTA, HAS_ONORM, K, NW, VPT>(row, q, mb, b, rank, warp, lane, c);
+  token_sums<S, HAS_DELTA, HAS_ONORM, K, NW, VPT>(row, c, q, mb, b, rank, warp, lane);
   token_mix<S, HAS_DELTA, HAS_ONORM, K, NW, VPT>(row, mb, b, parity, rank, warp, lane, eps, failed,
                                                  err, after_mix, c, acc);
   token_finish<S, HAS_DELTA, HAS_ONORM, K, NW, VPT>(mb, b, parity, lane, out_eps, failed, err, ow,

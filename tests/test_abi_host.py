@@ -45,7 +45,7 @@ def test_launch_shape(lib):
     ls = ar.launch_shape
     assert ls(1, 4, True) == dict(kernel="split", split=7, stages=0, threads=128, ctas=7, cluster=7)
     assert ls(64, 8, False) == dict(kernel="split", split=7, stages=0, threads=128, ctas=448, cluster=7)
-    assert ls(8192, 8, True) == dict(kernel="stream", split=4, stages=2, threads=128, ctas=0, cluster=4)
+    assert ls(8192, 8, True) == dict(kernel="stream", split=7, stages=2, threads=64, ctas=0, cluster=7)
     # no softmax and no output norm: the CTAs of a token never talk
     assert ls(1024, 0, False)["cluster"] == 1
     assert ls(2, 8, True, ar.FLAG_SPLIT(16)) == dict(kernel="split", split=16, stages=0, threads=64, ctas=32, cluster=16)
@@ -60,7 +60,7 @@ def test_launch_shape(lib):
                 (1, 1, 0, ar.FLAG_KERNEL(2) | ar.FLAG_STAGES(4)),
                 (1, 1, 0, ar.FLAG_KERNEL(2) | ar.FLAG_SPLIT(8) | ar.FLAG_VPT(2)),
                 (1, 1, 0, ar.FLAG_KERNEL(2) | ar.FLAG_STAGES(4)),
-                (1, 1, 0, ar.FLAG_KERNEL(2) | ar.FLAG_SPLIT(7) | ar.FLAG_STAGES(3)),
+                (1, 1, 0, ar.FLAG_KERNEL(2) | ar.FLAG_SPLIT(7) | ar.FLAG_VPT(1) | ar.FLAG_STAGES(3)),
                 (1, 1, 0, ar.FLAG_KERNEL(1) | ar.FLAG_VPT(2)),
                 (1, 1, 0, ar.FLAG_KERNEL(1) | ar.FLAG_STAGES(2)), (1, 1, 0, 1 << 30)]:
         with pytest.raises(ar.AttnResError):

@@ -184,7 +184,7 @@ def test_repeated_calls_are_deterministic():
 
 # ---- the persistent stream kernel ------------------------------------------------
 
-SHAPES = [(7, 1, 2), (7, 2, 2), (7, 4, 2), (4, 2, 2), (4, 4, 2), (4, 2, 3), (14, 2, 2), (2, 4, 2)]
+SHAPES = [(7, 1, 2), (7, 2, 2), (7, 2, 3), (7, 4, 2), (4, 2, 2), (4, 2, 3), (14, 1, 2), (14, 2, 2)]
 STREAM = [(S, sh) for S in range(9) for sh in SHAPES]
 
 
@@ -220,3 +220,26 @@ def test_split_kernel_at_prefill_size():
 def test_zz_device_status_clean():
     """No kernel recorded a stage-wait time-out during the tests above."""
     assert ar.device_status() == 0
+
+
+@pytest.mark.parametrize("kernel", [ar.KERNEL_SPLIT, ar.KERNEL_STREAM])
+def test_subnormal_current_row_is_correctly_rounded(kernel):
+    """c = bf16_rn(prefix + delta) must keep bf16 subnormals (no flush to
+    zero) and round ties to even, in both kernels: prefix and delta drawn
+    from subnormal and tiny normal bf16 values, S = 0 and no output norm, so
+    out == c bit for bit."""
+    rng = np.random.default_rng(12)
+    T = 130
+    wl = W.make_workload(T, 0, capacity=1, has_delta=True, has_out_norm=False,
+                         block_write_idx=0, seed=12)
+    mag = rng.integers(1, 0x0100, size=(T, wl.H)).astype(np.uint16)  # subnormals and the smallest normals
+    sign = (rng.random((T, wl.H)) < 0.5).astype(np.uint16) << 15
+    wl.prefix = mag | sign
+    mag = rng.integers(1, 0x0100, size=(T, wl.H)).astype(np.uint16)
+    sign = (rng.random((T, wl.H)) < 0.5).astype(np.uint16) << 15
+    wl.delta = mag | sign
+    ref = oracle.run_workload(wl, n_threads=NT)
+    gpu = G.run_gpu(wl, kernel=kernel)
+    assert np.array_equal(gpu["prefix"], ref["prefix"])
+    assert np.array_equal(gpu["bank"], ref["bank"])
+    assert np.array_equal(gpu["out"], ref["out"])
