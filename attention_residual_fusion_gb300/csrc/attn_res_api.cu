@@ -36,20 +36,26 @@ struct Plan {
   int shape;   // index into the stream kernel's shape table
 };
 
-// Few tokens: one cluster of 7 CTAs x 128 threads per token, all threads
-// active, so one token's latency chain (load, reduce, exchange) runs on 7 SMs
-// at once.
-// Many tokens: persistent clusters of 7 CTAs, 2 vectors per thread (64
-// threads per CTA, 6 CTAs per SM) and a 2-deep TMA ring -- the fastest
-// stream shape on GB300 from 256 to 8192 tokens.
-attn_res_status_t make_plan(int64_t T, uint32_t flags, Plan* out) {
+// Automatic choice (measured on GB300 over the prefill, decode and long
+// prefill workloads):
+//  * few tokens (T < 128), or no exchange at all (no bank rows and no output
+//    norm): the split kernel, 7 CTAs x 128 threads per token, all threads
+//    active, so a token's latency chain runs on 7 SMs at once;
+//  * otherwise the stream kernel: persistent clusters of 7 CTAs and a 2-deep
+//    TMA ring, with 4 vectors per thread (one warp per CTA, fewer warps and so
+//    less reduction and exchange work per token) when there are 6 or more bank
+//    rows or an output norm, else 2 vectors per thread (more warps per SM).
+attn_res_status_t make_plan(int64_t T, int num_blocks, bool has_onorm, uint32_t flags, Plan* out) {
   Plan pl;
   pl.kernel = static_cast<int>((flags >> 16) & 0xfu);
   pl.split = static_cast<int>((flags >> 8) & 0xffu);
   pl.stages = static_cast<int>((flags >> 20) & 0xfu);
   pl.vpt = static_cast<int>((flags >> 24) & 0xfu);
   pl.shape = -1;
-  if (pl.kernel == 0) pl.kernel = T >= kStreamMinTokens ? ATTN_RES_KERNEL_STREAM : ATTN_RES_KERNEL_SPLIT;
+  if (pl.kernel == 0) {
+    const bool exchange = num_blocks > 0 || has_onorm;
+    pl.kernel = (T >= kStreamMinTokens && exchange) ? ATTN_RES_KERNEL_STREAM : ATTN_RES_KERNEL_SPLIT;
+  }
   if (pl.kernel == ATTN_RES_KERNEL_SPLIT) {
     if (pl.split == 0) pl.split = 7;
     if (pl.vpt == 0) pl.vpt = 1;
@@ -57,7 +63,7 @@ attn_res_status_t make_plan(int64_t T, uint32_t flags, Plan* out) {
   } else if (pl.kernel == ATTN_RES_KERNEL_STREAM) {
     if (pl.split == 0) pl.split = 7;
     if (pl.stages == 0) pl.stages = 2;
-    if (pl.vpt == 0) pl.vpt = 2;
+    if (pl.vpt == 0) pl.vpt = (pl.split == 7 && (num_blocks >= 6 || has_onorm)) ? 4 : 2;
     pl.shape = stream_shape_index(pl.split, pl.vpt, pl.stages);
     if (pl.shape < 0) return ATTN_RES_EINVAL;
   } else {
@@ -198,7 +204,7 @@ attn_res_status_t attn_res_launch_shape(int64_t T, int num_blocks,
   if (T < 0 || num_blocks < 0 || num_blocks > ATTN_RES_MAX_BLOCKS) return ATTN_RES_EINVAL;
   if ((flags & ~kKnownFlags) != 0) return ATTN_RES_EINVAL;
   Plan pl;
-  attn_res_status_t st = make_plan(T, flags, &pl);
+  attn_res_status_t st = make_plan(T, num_blocks, has_out_norm != 0, flags, &pl);
   if (st != ATTN_RES_OK) return st;
   const bool comm = num_blocks > 0 || has_out_norm;
   if (kernel) *kernel = pl.kernel;
@@ -245,7 +251,8 @@ attn_res_status_t attn_res(attn_res_bf16_t* prefix, const attn_res_bf16_t* delta
     return ATTN_RES_EINVAL;
   if ((layout->flags & ~kKnownFlags) != 0) return ATTN_RES_EINVAL;
   Plan plan;
-  if (make_plan(T, layout->flags, &plan) != ATTN_RES_OK) return ATTN_RES_EINVAL;
+  if (make_plan(T, num_blocks, out_norm_w != nullptr, layout->flags, &plan) != ATTN_RES_OK)
+    return ATTN_RES_EINVAL;
   if (T * plan.split > INT32_MAX) return ATTN_RES_EINVAL;
   // no rows: nothing is read or written, so pointers and strides do not matter
   if (T == 0) return ATTN_RES_OK;

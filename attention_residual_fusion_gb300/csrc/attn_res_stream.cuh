@@ -45,13 +45,26 @@ struct StreamCfg {
   static constexpr uint32_t SLICE_BYTES = VPC * 16;  // one row's slice, multiple of 16
   static constexpr uint32_t STAGE_BYTES = S * SLICE_BYTES;
   static constexpr uint32_t SMEM_BYTES = STAGES * STAGE_BYTES;
+  // CTAs per SM that shared memory allows (ring, mailboxes, barriers and the
+  // 1 KB the system reserves per CTA, out of 228 KB), but never so many that
+  // a thread gets fewer registers than its VPT vectors need (64 + 48 per
+  // vector, at most 255): passed to __launch_bounds__ so the register budget
+  // matches the occupancy shared memory permits.
+  static constexpr uint32_t SMEM_PER_CTA =
+      SMEM_BYTES + sizeof(typename Tok::Box) + 16 * STAGES + 1024;
+  static constexpr int BY_SMEM = (int)(233472u / SMEM_PER_CTA);
+  static constexpr int REG_FLOOR = (64 + 48 * VPT) < 255 ? (64 + 48 * VPT) : 255;
+  static constexpr int BY_REGS = 65536 / (THREADS * REG_FLOOR);
+  static constexpr int MIN_BLOCKS_RAW = BY_SMEM < BY_REGS ? BY_SMEM : BY_REGS;
+  static constexpr int MIN_BLOCKS = MIN_BLOCKS_RAW < 1 ? 1 : MIN_BLOCKS_RAW;
   static_assert(kNV % K == 0, "split must divide the 896 row vectors");
   static_assert(VPC % VPT == 0, "vectors per thread must divide the slice");
   static_assert(STAGES >= 2 && STAGES <= 4, "ring depth");
 };
 
 template <int S, bool HAS_DELTA, bool HAS_ONORM, int K, int VPT, int STAGES>
-__global__ void __launch_bounds__(StreamCfg<S, HAS_DELTA, HAS_ONORM, K, VPT, STAGES>::THREADS)
+__global__ void __launch_bounds__(StreamCfg<S, HAS_DELTA, HAS_ONORM, K, VPT, STAGES>::THREADS,
+                                  StreamCfg<S, HAS_DELTA, HAS_ONORM, K, VPT, STAGES>::MIN_BLOCKS)
     attn_res_stream_kernel(const Params p, const int64_t T) {
   using C = StreamCfg<S, HAS_DELTA, HAS_ONORM, K, VPT, STAGES>;
   using Tok = typename C::Tok;

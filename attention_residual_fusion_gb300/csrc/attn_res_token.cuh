@@ -39,8 +39,16 @@ struct TokenCfg {
   static constexpr int N = S + 1;              // sources
   static constexpr int NR = 2 * N;             // partial sums per token
   static constexpr int ROWS = N + (HAS_DELTA ? 1 : 0);
-  static constexpr int P = pow2_at_least(NR);  // padded for the reduce-scatter
+  // The partial sums reduce as one power-of-two butterfly of P values, plus
+  // a second one of P2 values when NR is just above a power of two (NR = 18
+  // for S = 8 reduces as 16 + 2 instead of a padded 32).
+  static constexpr int P_FULL = pow2_at_least(NR);
+  static constexpr int P = (NR > 16) ? 16 : P_FULL;
+  static constexpr int NR2 = NR - P > 0 ? NR - P : 0;  // values in the second butterfly
+  static constexpr int P2 = NR2 > 0 ? pow2_at_least(NR2) : 1;
   static constexpr int SHIFT = 5 - log2_exact(P);
+  static constexpr int SHIFT2 = 5 - log2_exact(P2);
+  static_assert(NR2 <= 16, "second butterfly too large");
   static constexpr uint32_t SUMS_BYTES = K * NW * NR * 4;  // expected per token
   static constexpr uint32_t SQ_BYTES = K * NW * 4;
   static constexpr bool COMM = (S > 0) || HAS_ONORM;
@@ -106,9 +114,10 @@ __device__ __forceinline__ void token_sums(Row row, const uint4 (&c)[VPT],
   constexpr int P = C::P;
   if constexpr (S > 0) {
     // per-source partial sums over this thread's columns
-    float part[P];
+    constexpr int P2 = C::P2;
+    float part[P + P2];
 #pragma unroll
-    for (int r = 0; r < P; ++r) part[r] = 0.f;
+    for (int r = 0; r < P + P2; ++r) part[r] = 0.f;
 #pragma unroll
     for (int i = 0; i < N; ++i) {
       f32x2 ss = 0ull, dt = 0ull;  // +0.0f pairs
@@ -126,14 +135,29 @@ __device__ __forceinline__ void token_sums(Row row, const uint4 (&c)[VPT],
       part[N + i] = f2_lo(dt) + f2_hi(dt);
     }
     // warp totals, then into every CTA's mailbox
-    const float tv = reduce_scatter<P>(part, lane);
+    const int src = (int)rank * NW + warp;
+    const uint32_t bar = smem_addr(&mb.bar_sums[b]);
+    float lo[P];
+#pragma unroll
+    for (int r = 0; r < P; ++r) lo[r] = part[r];
+    const float tv = reduce_scatter<P>(lo, lane);
     const int idx = lane >> C::SHIFT;
-    if ((lane & ((1 << C::SHIFT) - 1)) == 0 && idx < NR) {
-      const int src = (int)rank * NW + warp;
+    if ((lane & ((1 << C::SHIFT) - 1)) == 0 && idx < (NR < P ? NR : P)) {
       const uint32_t a = smem_addr(&mb.sums[b][src][idx]);
-      const uint32_t bar = smem_addr(&mb.bar_sums[b]);
 #pragma unroll
       for (int r = 0; r < K; ++r) st_async_f32(map_rank(a, r), tv, map_rank(bar, r));
+    }
+    if constexpr (C::NR2 > 0) {
+      float hi[P2];
+#pragma unroll
+      for (int r = 0; r < P2; ++r) hi[r] = part[P + r];
+      const float tv2 = reduce_scatter<P2>(hi, lane);
+      const int idx2 = lane >> C::SHIFT2;
+      if ((lane & ((1 << C::SHIFT2) - 1)) == 0 && idx2 < C::NR2) {
+        const uint32_t a = smem_addr(&mb.sums[b][src][P + idx2]);
+#pragma unroll
+        for (int r = 0; r < K; ++r) st_async_f32(map_rank(a, r), tv2, map_rank(bar, r));
+      }
     }
   }
 }

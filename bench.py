@@ -16,6 +16,8 @@ than L2, so no flush is needed between steps.
              HBM copy bandwidth
   latency_us T=1 latency (single-token and 8-block cases): per call with an
              L2 flush in between, and back-to-back in a CUDA graph
+  prefill_cells  T=1024/2048 prefill cells: µs per call from CUDA-graph
+             replay, cycling through input copies larger than 3x L2
   cpu_baseline  the CPU oracle on a bounded sample of the same workload
 
 ``--impl reference`` times the CPU oracle on the same workload and metric.
@@ -245,6 +247,64 @@ def time_device(ar, wl, t, torch, stream, steps, warmup):
     return ev[0].elapsed_time(ev[steps]), per
 
 
+def input_sets(wl, t, torch, dev):
+    """The device inputs plus extra copies, so that cycling through them
+    touches at least 3x the L2 size: every launch then reads from HBM."""
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    n = min(16, max(1, -(-3 * l2 // wl.algorithmic_bytes())))
+    sets = [t]
+    for _ in range(n - 1):
+        sets.append({k: (v.clone() if v is not None and k in ("prefix", "delta", "bank", "out") else v)
+                     for k, v in t.items()})
+    return sets
+
+
+def time_graph(ar, wl, sets, torch, stream, calls=64):
+    """Mean µs per call of `calls` back-to-back launches replayed from a CUDA
+    graph (no host launch overhead), cycling through the input sets."""
+    for st in sets:
+        call(ar, wl, st, stream)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for i in range(calls):
+            call(ar, wl, sets[i % len(sets)], stream)
+    g.replay()
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        a.record(stream)
+        g.replay()
+        b.record(stream)
+    torch.cuda.synchronize()
+    del g
+    return a.elapsed_time(b) * 1e3 / calls
+
+
+SWEEP = ["prefill:1024:0:1:7", "prefill:1024:4:1:7", "prefill:1024:8:1:7",
+         "prefill:2048:0:1:7", "prefill:2048:4:1:7", "prefill:2048:8:1:7"]
+
+
+def sweep_prefill(ar, torch, dev, stream, peak):
+    """The other T >= 1024 cells (prefill workloads): µs per call from graph
+    replay over rotating input sets larger than 3x L2."""
+    rows = []
+    for name in SWEEP:
+        wl, _ = make(name)
+        t = device_tensors(wl, torch, dev)
+        sets = input_sets(wl, t, torch, dev)
+        us = time_graph(ar, wl, sets, torch, stream)
+        gbs = wl.algorithmic_bytes() / (us * 1e-6) / 1e9
+        rows.append({"workload": name, "us_per_call": round(us, 2),
+                     "tokens_per_s": round(wl.T / (us * 1e-6), 1),
+                     "gbs": round(gbs, 1), "frac": round(gbs / peak, 4),
+                     "input_sets": len(sets)})
+        del t, sets
+        torch.cuda.empty_cache()
+    return rows
+
+
 def latency_t1(ar, torch, dev, stream, reps=200):
     """T=1 latency: per call with L2 flushed between calls (events around each
     call), and back-to-back inside a captured CUDA graph."""
@@ -401,8 +461,13 @@ def run_ours(args, rank, world, local_rank, dist):
     }
     if rank == 0 and not args.no_latency:
         line["latency_us"] = latency_t1(ar, torch, dev, stream)
-    if not args.no_e2e:
+    if rank == 0 and not args.no_sweep:
         del t
+        torch.cuda.empty_cache()
+        line["prefill_cells"] = sweep_prefill(ar, torch, dev, stream, peak)
+        t = None
+    if not args.no_e2e:
+        t = None
         torch.cuda.empty_cache()
         e = e2e(ar, wl, torch, dev, stream, max(3, min(args.steps, args.e2e_steps)))
         if dist is not None:
@@ -471,6 +536,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-latency", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-sweep", action="store_true", help="skip the prefill T=1024/2048 cells")
     args = ap.parse_args()
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
