@@ -42,7 +42,8 @@ STATUS = {0: "ATTN_RES_OK", 1: "ATTN_RES_EINVAL", 2: "ATTN_RES_EALIGN",
 
 # Every symbol the header declares.
 EXPORTS = ("attn_res", "attn_res_status_string", "attn_res_hidden_size",
-           "attn_res_max_blocks", "attn_res_launch_shape", "attn_res_device_status")
+           "attn_res_max_blocks", "attn_res_launch_shape", "attn_res_device_status",
+           "attn_res_selftest_wait_timeout")
 
 
 class Layout(ctypes.Structure):
@@ -93,6 +94,8 @@ def lib():
             ip, ip, ip, ip, ctypes.POINTER(ctypes.c_int64), ip]
         L.attn_res_device_status.restype = ctypes.c_int
         L.attn_res_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint), ctypes.c_int]
+        L.attn_res_selftest_wait_timeout.restype = ctypes.c_int
+        L.attn_res_selftest_wait_timeout.argtypes = [ctypes.c_uint, ctypes.POINTER(ctypes.c_uint)]
         _lib = L
     return _lib
 
@@ -120,6 +123,15 @@ def device_status(clear: bool = False) -> int:
     """Error bits recorded by the kernels on the current device (0 = none)."""
     bits = ctypes.c_uint()
     st = lib().attn_res_device_status(ctypes.byref(bits), int(clear))
+    if st != 0:
+        raise AttnResError(st, status_string(st))
+    return bits.value
+
+
+def selftest_wait_timeout(limit_us: int) -> int:
+    """Run the bounded-wait self-test; returns the device status word."""
+    bits = ctypes.c_uint()
+    st = lib().attn_res_selftest_wait_timeout(limit_us, ctypes.byref(bits))
     if st != 0:
         raise AttnResError(st, status_string(st))
     return bits.value

@@ -162,6 +162,21 @@ StreamLaunchFn lookup_stream(int S, int shape, bool d, bool o) {
   }
 }
 
+// Self-test of the bounded waits: one warp waits, with the same code the
+// mixture kernels use, on an mbarrier that nothing ever arrives at; the wait
+// must give up after limit_ns and record the stage time-out bit.
+__global__ void attn_res_selftest_wait_kernel(unsigned* err, uint64_t limit_ns) {
+  __shared__ __align__(8) unsigned long long bar;
+  if (threadIdx.x == 0) {
+    attn_res_dev::mbar_init(attn_res_dev::smem_addr(&bar), 1);
+    attn_res_dev::fence_mbar_init();
+  }
+  __syncthreads();
+  if (!attn_res_dev::mbar_wait_bounded(attn_res_dev::smem_addr(&bar), 0u, limit_ns) &&
+      threadIdx.x == 0)
+    atomicOr(err, attn_res_dev::kErrStageTimeout);
+}
+
 LaunchFn lookup(int S, int split_idx, bool d, bool o) {
   switch (S) {
     case 0: return launcher_s0(split_idx, d, o);
@@ -213,6 +228,29 @@ attn_res_status_t attn_res_launch_shape(int64_t T, int num_blocks,
   if (threads_per_cta) *threads_per_cta = threads_for(pl.split, pl.vpt);
   if (ctas) *ctas = pl.kernel == ATTN_RES_KERNEL_SPLIT ? T * pl.split : 0;
   if (cluster) *cluster = comm ? pl.split : 1;
+  return ATTN_RES_OK;
+}
+
+attn_res_status_t attn_res_selftest_wait_timeout(unsigned int limit_us, unsigned int* bits) {
+  if (bits == nullptr || limit_us == 0 || limit_us > 1000000u) return ATTN_RES_EINVAL;
+  int dev = 0;
+  attn_res_status_t st = check_device(&dev);
+  if (st != ATTN_RES_OK) return st;
+  unsigned* w = nullptr;
+  cudaStream_t s = nullptr;
+  cudaError_t e = status_word(dev, &w);
+  if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking);
+  if (e == cudaSuccess) {
+    attn_res_selftest_wait_kernel<<<1, 32, 0, s>>>(w, (uint64_t)limit_us * 1000u);
+    e = cudaGetLastError();
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e == cudaSuccess) e = cudaMemcpy(bits, w, sizeof(unsigned), cudaMemcpyDeviceToHost);
+  }
+  if (s != nullptr) (void)cudaStreamDestroy(s);
+  if (e != cudaSuccess) {
+    (void)cudaGetLastError();
+    return ATTN_RES_ECUDA;
+  }
   return ATTN_RES_OK;
 }
 

@@ -116,14 +116,15 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
   return t;
 }
 // Wait for the phase of parity `parity` of an mbarrier of this CTA, at most
-// about kWaitLimitNs.  Returns false on time-out.  The clock is read once at
-// the first miss and then every 1024 tries.
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
+// about limit_ns.  Returns false on time-out.  The clock is read once at the
+// first miss and then every 1024 tries.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
+                                                  uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 1023u) == 0 && global_timer_ns() - t0 > kWaitLimitNs) return false;
+    if ((it & 1023u) == 0 && global_timer_ns() - t0 > limit_ns) return false;
   }
 }
 // Waits unless an earlier wait of this thread already failed; records the

@@ -21,6 +21,8 @@
 //     `empty` mbarrier; thread 0 waits on it, fences the generic-proxy reads
 //     against the async proxy and refills the stage with the token STAGES
 //     ahead;
+//   * dependents of a PDL launch are released only when this CTA has run
+//     out of tokens (the grid holds every SM until then);
 //   * the token phases run software-pipelined: B(j) (softmax, mix), refill,
 //     A(j+1) (partial sums of the next token), C(j) (output norm, stores), so
 //     one token's exchanges overlap the next token's work.
@@ -158,7 +160,6 @@ __global__ void __launch_bounds__(StreamCfg<S, HAS_DELTA, HAS_ONORM, K, VPT, STA
   grid_dep_wait();  // every thread: also orders our stores after the producer's work
   uint4 pre[VPT], del[VPT];  // prefix and delta of the next token to start
   if (ntok > 0) load_current(cid, pre, del);
-  grid_dep_launch_dependents();
 
   f32x2 q[VPT][4];
   make_query<VPT>(rw, qw, q);
@@ -240,6 +241,11 @@ __global__ void __launch_bounds__(StreamCfg<S, HAS_DELTA, HAS_ONORM, K, VPT, STA
       c_cur[v] = c_next[v];
     }
   }
+
+  // This grid occupies every SM until its clusters run out of tokens: let a
+  // dependent grid launch only now, so its prologue overlaps our tail instead
+  // of taking SM slots from clusters still streaming.
+  grid_dep_launch_dependents();
 
   // After a time-out, do not leave with copies still landing in shared memory.
   if (tid == 0 && failed) {

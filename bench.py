@@ -16,6 +16,8 @@ than L2, so no flush is needed between steps.
              HBM copy bandwidth
   latency_us T=1 latency (single-token and 8-block cases): per call with an
              L2 flush in between, and back-to-back in a CUDA graph
+  pdl_chain  graph-replayed chains of calls with and without programmatic
+             dependent launch (T=1 and T=1024)
   prefill_cells  T=1024/2048 prefill cells: µs per call from CUDA-graph
              replay, cycling through input copies larger than 3x L2
   cpu_baseline  the CPU oracle on a bounded sample of the same workload
@@ -305,6 +307,46 @@ def sweep_prefill(ar, torch, dev, stream, peak):
     return rows
 
 
+def pdl_chain(ar, torch, dev, stream):
+    """Back-to-back calls replayed from a CUDA graph, with and without
+    programmatic dependent launch (each call's bank-row and weight loads may
+    then overlap the previous call's tail).  Workloads without a bank
+    write-back, so a call never reads, before its grid-dependency wait, data
+    the previous call writes."""
+    out = {}
+    for name in ("single_token", "prefill:1024:8:1:-1"):
+        wl, _ = make(name)
+        t = device_tensors(wl, torch, dev)
+        sets = input_sets(wl, t, torch, dev)
+        row = {}
+        for pdl in (False, True):
+            for st in sets:
+                call(ar, wl, st, stream, pdl=pdl)
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            n = 64
+            with torch.cuda.graph(g, stream=stream):
+                for i in range(n):
+                    call(ar, wl, sets[i % len(sets)], stream, pdl=pdl)
+            g.replay()
+            torch.cuda.synchronize()
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(stream):
+                a.record(stream)
+                for _ in range(4):
+                    g.replay()
+                b.record(stream)
+            torch.cuda.synchronize()
+            row["pdl_us_per_call" if pdl else "us_per_call"] = round(a.elapsed_time(b) * 1e3 / (4 * n), 3)
+            del g
+        row["input_sets"] = len(sets)
+        out[name] = row
+        del t, sets
+        torch.cuda.empty_cache()
+    return out
+
+
 def latency_t1(ar, torch, dev, stream, reps=200):
     """T=1 latency: per call with L2 flushed between calls (events around each
     call), and back-to-back inside a captured CUDA graph."""
@@ -461,6 +503,8 @@ def run_ours(args, rank, world, local_rank, dist):
     }
     if rank == 0 and not args.no_latency:
         line["latency_us"] = latency_t1(ar, torch, dev, stream)
+    if rank == 0 and not args.no_latency:
+        line["pdl_chain"] = pdl_chain(ar, torch, dev, stream)
     if rank == 0 and not args.no_sweep:
         del t
         torch.cuda.empty_cache()

@@ -178,6 +178,17 @@ attn_res_status_t attn_res_launch_shape(int64_t T, int num_blocks,
  */
 attn_res_status_t attn_res_device_status(unsigned int* bits, int clear);
 
+/*
+ * attn_res_selftest_wait_timeout -- exercise the kernels' time-out path on
+ * the current device: one warp waits, with the same bounded-wait code the
+ * mixture kernels use, on an mbarrier that nothing ever completes; after
+ * about `limit_us` microseconds (1 .. 1 000 000) the wait gives up and bit 0
+ * of the device status word is set.  Synchronous: returns after the kernel
+ * finished, with the status word (not cleared) in *bits.  A diagnostic for
+ * tests; it does not touch any caller buffer.
+ */
+attn_res_status_t attn_res_selftest_wait_timeout(unsigned int limit_us, unsigned int* bits);
+
 #ifdef __cplusplus
 }
 #endif

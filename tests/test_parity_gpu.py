@@ -243,3 +243,37 @@ def test_subnormal_current_row_is_correctly_rounded(kernel):
     assert np.array_equal(gpu["prefix"], ref["prefix"])
     assert np.array_equal(gpu["bank"], ref["bank"])
     assert np.array_equal(gpu["out"], ref["out"])
+
+
+@pytest.mark.parametrize("T", [1, 300])
+def test_pdl_chain_in_graph(T):
+    """Three dependent calls captured in a CUDA graph with programmatic
+    dependent launch: each call updates prefix in place and the next reads it
+    after its grid-dependency wait.  Equal to applying the oracle three
+    times."""
+    import torch
+    wl = W.make_workload(T, 6, capacity=8, has_delta=True, has_out_norm=True,
+                         block_write_idx=-1, seed=30 + T, mixing=True)
+    ref_wl = wl.copy()
+    for _ in range(3):
+        r = oracle.run_workload(ref_wl, n_threads=NT)
+        ref_wl.prefix = r["prefix"]
+    up = lambda a: torch.from_numpy(a.view(np.int16)).cuda().view(torch.bfloat16)
+    down = lambda t: t.cpu().view(torch.int16).numpy().view(np.uint16)
+    d = dict(prefix=up(wl.prefix), delta=up(wl.delta), bank=up(wl.bank), rms=up(wl.rms_w),
+             res=up(wl.res_w), onw=up(wl.out_norm_w))
+    out = torch.empty_like(d["prefix"])
+    s = torch.cuda.Stream()
+    args = (d["prefix"], d["delta"], d["bank"], 6, -1, d["res"], d["rms"], d["onw"], 1e-6, 1e-6, out)
+    ar.attn_res(*args, pdl=True, stream=s)   # one-time set-up outside capture
+    torch.cuda.synchronize()
+    d["prefix"].copy_(up(wl.prefix))
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for _ in range(3):
+            ar.attn_res(*args, pdl=True, stream=s)
+    g.replay()
+    torch.cuda.synchronize()
+    assert np.array_equal(down(d["prefix"]), r["prefix"])
+    G.assert_out_close(down(out), r["out"], "pdl-chain")
