@@ -19,6 +19,7 @@ MAX_BLOCKS = 8
 FLAG_PDL = 0x1
 KERNEL_SPLIT = 1
 KERNEL_STREAM = 2
+KERNEL_GENERIC = 3
 
 
 def FLAG_SPLIT(k: int) -> int:
@@ -43,7 +44,7 @@ STATUS = {0: "ATTN_RES_OK", 1: "ATTN_RES_EINVAL", 2: "ATTN_RES_EALIGN",
 # Every symbol the header declares.
 EXPORTS = ("attn_res", "attn_res_status_string", "attn_res_hidden_size",
            "attn_res_max_blocks", "attn_res_launch_shape", "attn_res_device_status",
-           "attn_res_selftest_wait_timeout")
+           "attn_res_selftest_wait_timeout", "attn_res_h")
 
 
 class Layout(ctypes.Structure):
@@ -81,6 +82,8 @@ def lib():
         L.attn_res.argtypes = [vp, vp, vp, ctypes.c_int, ctypes.c_int, vp, vp, vp,
                                ctypes.c_float, ctypes.c_float, vp, ctypes.c_int64,
                                ctypes.POINTER(Layout), vp]
+        L.attn_res_h.restype = ctypes.c_int
+        L.attn_res_h.argtypes = [ctypes.c_int64] + L.attn_res.argtypes
         L.attn_res_status_string.restype = ctypes.c_char_p
         L.attn_res_status_string.argtypes = [ctypes.c_int]
         L.attn_res_hidden_size.restype = ctypes.c_int
@@ -115,7 +118,7 @@ def launch_shape(T: int, num_blocks: int, has_out_norm: bool, flags: int = 0) ->
                                      ctypes.byref(ctas), ctypes.byref(cl))
     if st != 0:
         raise AttnResError(st, status_string(st))
-    return dict(kernel={1: "split", 2: "stream"}[kern.value], split=k.value,
+    return dict(kernel={1: "split", 2: "stream", 3: "generic"}[kern.value], split=k.value,
                 stages=st_.value, threads=th.value, ctas=ctas.value, cluster=cl.value)
 
 
@@ -140,12 +143,15 @@ def selftest_wait_timeout(limit_us: int) -> int:
 def call_raw(prefix: int, delta: int, blocks: int, num_blocks: int,
              block_write_idx: int, res_w: int, rms_w: int, out_norm_w: int,
              eps: float, out_eps: float, out: int, T: int, layout: Layout,
-             stream: int) -> int:
-    """The C entry point on raw addresses; returns the status code."""
-    return lib().attn_res(prefix or None, delta or None, blocks or None,
-                          num_blocks, block_write_idx, res_w or None,
-                          rms_w or None, out_norm_w or None, eps, out_eps,
-                          out or None, T, ctypes.byref(layout), stream or None)
+             stream: int, H: int = HIDDEN) -> int:
+    """The C entry point on raw addresses (attn_res, or attn_res_h when H is
+    not the built-in width); returns the status code."""
+    args = (prefix or None, delta or None, blocks or None, num_blocks,
+            block_write_idx, res_w or None, rms_w or None, out_norm_w or None,
+            eps, out_eps, out or None, T, ctypes.byref(layout), stream or None)
+    if H == HIDDEN:
+        return lib().attn_res(*args)
+    return lib().attn_res_h(H, *args)
 
 
 def _ptr(t) -> int:
@@ -157,7 +163,8 @@ def attn_res(prefix, delta, blocks, num_blocks: int, block_write_idx: int,
              out_eps: float = 1e-6, out=None, *, pdl: bool = False,
              split: int = 0, kernel: int = 0, stages: int = 0, vpt: int = 0,
              stream=None):
-    """AttnRes mixture on CUDA bf16 tensors (see include/attn_res.h).
+    """AttnRes mixture on CUDA bf16 tensors (see include/attn_res.h); H is
+    the length of ``res_w`` (7168 for the tuned kernels, any multiple of 8).
 
     prefix [T, H] (updated in place when ``delta`` is given), delta [T, H] or
     None, blocks [T, capacity, H] (any token/slot strides, unit inner stride;
@@ -172,8 +179,9 @@ def attn_res(prefix, delta, blocks, num_blocks: int, block_write_idx: int,
         if t is not None and (t.dtype != torch.bfloat16 or t.device.type != "cuda"):
             raise ValueError(f"{name} must be a CUDA bfloat16 tensor")
     T = prefix.shape[0]
+    H = res_w.shape[0]
     if out is None:
-        out = torch.empty((T, HIDDEN), dtype=prefix.dtype, device=prefix.device)
+        out = torch.empty((T, H), dtype=prefix.dtype, device=prefix.device)
     for name, t in (("prefix", prefix), ("delta", delta), ("out", out)):
         if t is not None and (t.dim() != 2 or t.stride(1) != 1):
             raise ValueError(f"{name} must be a [T, H] tensor with unit inner stride")
@@ -191,7 +199,7 @@ def attn_res(prefix, delta, blocks, num_blocks: int, block_write_idx: int,
         stream = torch.cuda.current_stream(prefix.device)
     st = call_raw(_ptr(prefix), _ptr(delta), _ptr(blocks), num_blocks,
                   block_write_idx, _ptr(res_w), _ptr(rms_w), _ptr(out_norm_w),
-                  eps, out_eps, _ptr(out), T, lay, int(stream.cuda_stream))
+                  eps, out_eps, _ptr(out), T, lay, int(stream.cuda_stream), H)
     if st != 0:
         raise AttnResError(st, status_string(st))
     return out

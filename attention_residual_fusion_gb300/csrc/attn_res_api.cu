@@ -60,6 +60,9 @@ attn_res_status_t make_plan(int64_t T, int num_blocks, bool has_onorm, uint32_t 
     if (pl.split == 0) pl.split = 7;
     if (pl.vpt == 0) pl.vpt = 1;
     if (split_index(pl.split) < 0 || pl.stages != 0 || pl.vpt != 1) return ATTN_RES_EINVAL;
+  } else if (pl.kernel == ATTN_RES_KERNEL_GENERIC) {
+    if (pl.split != 0 || pl.stages != 0 || pl.vpt != 0) return ATTN_RES_EINVAL;
+    pl.split = 1;
   } else if (pl.kernel == ATTN_RES_KERNEL_STREAM) {
     if (pl.split == 0) pl.split = 7;
     if (pl.stages == 0) pl.stages = 2;
@@ -86,10 +89,10 @@ struct Region {
   bool written;
 };
 
-Region rows_region(const void* p, int64_t T, int64_t row, bool used, bool written) {
+Region rows_region(const void* p, int64_t T, int64_t row, int64_t H, bool used, bool written) {
   Region r{0, 0, used && p != nullptr, written};
   if (r.used) {
-    const int64_t elems = (T - 1) * row + kH;
+    const int64_t elems = (T - 1) * row + H;
     r.lo = reinterpret_cast<uintptr_t>(p);
     r.hi = r.lo + static_cast<uintptr_t>(elems) * 2u;
   }
@@ -147,6 +150,21 @@ attn_res_status_t check_device(int* dev_out) {
   return st == 1 ? ATTN_RES_OK : ATTN_RES_EDEVICE;
 }
 
+GenericLaunchFn lookup_generic(int S, bool d, bool o) {
+  switch (S) {
+    case 0: return generic_launcher_s0(d, o);
+    case 1: return generic_launcher_s1(d, o);
+    case 2: return generic_launcher_s2(d, o);
+    case 3: return generic_launcher_s3(d, o);
+    case 4: return generic_launcher_s4(d, o);
+    case 5: return generic_launcher_s5(d, o);
+    case 6: return generic_launcher_s6(d, o);
+    case 7: return generic_launcher_s7(d, o);
+    case 8: return generic_launcher_s8(d, o);
+    default: return nullptr;
+  }
+}
+
 StreamLaunchFn lookup_stream(int S, int shape, bool d, bool o) {
   switch (S) {
     case 0: return stream_launcher_s0(shape, d, o);
@@ -192,6 +210,121 @@ LaunchFn lookup(int S, int split_idx, bool d, bool o) {
   }
 }
 
+attn_res_status_t run(int64_t H, attn_res_bf16_t* prefix, const attn_res_bf16_t* delta,
+                      attn_res_bf16_t* blocks, int num_blocks, int block_write_idx,
+                      const attn_res_bf16_t* res_w, const attn_res_bf16_t* rms_w,
+                      const attn_res_bf16_t* out_norm_w, float eps, float out_eps,
+                      attn_res_bf16_t* out, int64_t T, const attn_res_layout_t* layout,
+                      void* stream) {
+  // ---- arguments (pure host checks, no CUDA call) ----
+  if (layout == nullptr || T < 0) return ATTN_RES_EINVAL;
+  if (H <= 0 || H % 8 != 0 || H > kMaxStride) return ATTN_RES_EINVAL;
+  const int cap = layout->blocks_capacity;
+  if (num_blocks < 0 || num_blocks > ATTN_RES_MAX_BLOCKS || cap < 0 || num_blocks > cap)
+    return ATTN_RES_EINVAL;
+  if (block_write_idx < -1 || block_write_idx >= cap) return ATTN_RES_EINVAL;
+  if (!std::isfinite(eps) || eps < 0.f || !std::isfinite(out_eps) || out_eps < 0.f)
+    return ATTN_RES_EINVAL;
+  if ((layout->flags & ~kKnownFlags) != 0) return ATTN_RES_EINVAL;
+  Plan plan;
+  if (make_plan(T, num_blocks, out_norm_w != nullptr, layout->flags, &plan) != ATTN_RES_OK)
+    return ATTN_RES_EINVAL;
+  // widths other than the one the fast kernels are built for take the
+  // general kernel
+  if (H != kH) {
+    const int forced = static_cast<int>((layout->flags >> 16) & 0xfu);
+    if (forced != 0 && forced != ATTN_RES_KERNEL_GENERIC) return ATTN_RES_EINVAL;
+    plan.kernel = ATTN_RES_KERNEL_GENERIC;
+  }
+  if (plan.kernel == ATTN_RES_KERNEL_GENERIC) plan.split = 1;
+  if (T * plan.split > INT32_MAX) return ATTN_RES_EINVAL;
+  // no rows: nothing is read or written, so pointers and strides do not matter
+  if (T == 0) return ATTN_RES_OK;
+
+  const bool has_delta = delta != nullptr;
+  const bool has_onorm = out_norm_w != nullptr;
+  const bool uses_bank = num_blocks > 0 || block_write_idx >= 0;
+  if (!prefix || !res_w || !rms_w || !out || (uses_bank && !blocks)) return ATTN_RES_EINVAL;
+
+  const int64_t pr = layout->prefix_row, dr = layout->delta_row, bt = layout->blocks_token,
+                bs = layout->blocks_slot, orow = layout->out_row;
+  auto bad_row_stride = [H](int64_t s) { return s < H || s > kMaxStride; };
+  if (bad_row_stride(pr) || bad_row_stride(orow) || (has_delta && bad_row_stride(dr)))
+    return ATTN_RES_EINVAL;
+  if (uses_bank) {
+    if (bad_row_stride(bs)) return ATTN_RES_EINVAL;
+    if (T > 1 && (bt < (int64_t)(cap - 1) * bs + H || bt > kMaxStride)) return ATTN_RES_EINVAL;
+  }
+  if (!aligned16(prefix) || !aligned16(res_w) || !aligned16(rms_w) || !aligned16(out) ||
+      (has_delta && !aligned16(delta)) || (has_onorm && !aligned16(out_norm_w)) ||
+      (uses_bank && !aligned16(blocks)))
+    return ATTN_RES_EALIGN;
+  if ((pr % 8) || (orow % 8) || (has_delta && (dr % 8)) || (uses_bank && ((bs % 8) || (bt % 8))))
+    return ATTN_RES_EALIGN;
+
+  {
+    const int64_t bank_elems = (T - 1) * (T > 1 ? bt : 0) + (int64_t)(cap > 0 ? cap - 1 : 0) * bs + H;
+    Region regs[7] = {
+        rows_region(prefix, T, pr, H, true, has_delta),
+        rows_region(delta, T, dr, H, has_delta, false),
+        Region{reinterpret_cast<uintptr_t>(blocks),
+               reinterpret_cast<uintptr_t>(blocks) + static_cast<uintptr_t>(bank_elems) * 2u,
+               uses_bank, block_write_idx >= 0},
+        rows_region(res_w, 1, H, H, true, false),
+        rows_region(rms_w, 1, H, H, true, false),
+        rows_region(out_norm_w, 1, H, H, has_onorm, false),
+        rows_region(out, T, orow, H, true, true),
+    };
+    for (int i = 0; i < 7; ++i)
+      for (int j = 0; j < 7; ++j)
+        if (i != j && regs[i].written && overlaps(regs[i], regs[j])) return ATTN_RES_EALIAS;
+  }
+
+  // ---- device and launch ----
+  int dev = 0;
+  attn_res_status_t st = check_device(&dev);
+  if (st != ATTN_RES_OK) return st;
+
+  Params p;
+  p.prefix = prefix;
+  p.delta = delta;
+  p.blocks = blocks;
+  p.res_w = res_w;
+  p.rms_w = rms_w;
+  p.onw = out_norm_w;
+  p.out = out;
+  p.prefix_row = pr;
+  p.delta_row = has_delta ? dr : 0;
+  p.blocks_token = uses_bank ? bt : 0;
+  p.blocks_slot = uses_bank ? bs : 0;
+  p.out_row = orow;
+  p.write_idx = block_write_idx;
+  p.eps = eps;
+  p.out_eps = out_eps;
+  const bool pdl = (layout->flags & ATTN_RES_FLAG_PDL) != 0;
+  cudaError_t e = status_word(dev, &p.err);
+  if (e == cudaSuccess) {
+    if (plan.kernel == ATTN_RES_KERNEL_GENERIC) {
+      GenericLaunchFn fn = lookup_generic(num_blocks, has_delta, has_onorm);
+      if (fn == nullptr) return ATTN_RES_EINVAL;
+      e = fn(p, T, H, pdl, static_cast<cudaStream_t>(stream));
+    } else if (plan.kernel == ATTN_RES_KERNEL_SPLIT) {
+      LaunchFn fn = lookup(num_blocks, split_index(plan.split), has_delta, has_onorm);
+      if (fn == nullptr) return ATTN_RES_EINVAL;
+      e = fn(p, T, pdl, static_cast<cudaStream_t>(stream), dev);
+    } else {
+      StreamLaunchFn fn = lookup_stream(num_blocks, plan.shape, has_delta, has_onorm);
+      if (fn == nullptr) return ATTN_RES_EINVAL;
+      e = fn(p, T, pdl, static_cast<cudaStream_t>(stream), dev);
+    }
+  }
+  if (e != cudaSuccess) {
+    (void)cudaGetLastError();
+    return ATTN_RES_ECUDA;
+  }
+  return ATTN_RES_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -222,12 +355,14 @@ attn_res_status_t attn_res_launch_shape(int64_t T, int num_blocks,
   attn_res_status_t st = make_plan(T, num_blocks, has_out_norm != 0, flags, &pl);
   if (st != ATTN_RES_OK) return st;
   const bool comm = num_blocks > 0 || has_out_norm;
+  const bool generic = pl.kernel == ATTN_RES_KERNEL_GENERIC;
   if (kernel) *kernel = pl.kernel;
   if (split) *split = pl.split;
   if (stages) *stages = pl.stages;
-  if (threads_per_cta) *threads_per_cta = threads_for(pl.split, pl.vpt);
-  if (ctas) *ctas = pl.kernel == ATTN_RES_KERNEL_SPLIT ? T * pl.split : 0;
-  if (cluster) *cluster = comm ? pl.split : 1;
+  if (threads_per_cta)
+    *threads_per_cta = generic ? attn_res_dev::kGenericThreads : threads_for(pl.split, pl.vpt);
+  if (ctas) *ctas = pl.kernel == ATTN_RES_KERNEL_STREAM ? 0 : T * pl.split;
+  if (cluster) *cluster = (comm && !generic) ? pl.split : 1;
   return ATTN_RES_OK;
 }
 
@@ -279,100 +414,18 @@ attn_res_status_t attn_res(attn_res_bf16_t* prefix, const attn_res_bf16_t* delta
                            const attn_res_bf16_t* out_norm_w, float eps,
                            float out_eps, attn_res_bf16_t* out, int64_t T,
                            const attn_res_layout_t* layout, void* stream) {
-  // ---- arguments (pure host checks, no CUDA call) ----
-  if (layout == nullptr || T < 0) return ATTN_RES_EINVAL;
-  const int cap = layout->blocks_capacity;
-  if (num_blocks < 0 || num_blocks > ATTN_RES_MAX_BLOCKS || cap < 0 || num_blocks > cap)
-    return ATTN_RES_EINVAL;
-  if (block_write_idx < -1 || block_write_idx >= cap) return ATTN_RES_EINVAL;
-  if (!std::isfinite(eps) || eps < 0.f || !std::isfinite(out_eps) || out_eps < 0.f)
-    return ATTN_RES_EINVAL;
-  if ((layout->flags & ~kKnownFlags) != 0) return ATTN_RES_EINVAL;
-  Plan plan;
-  if (make_plan(T, num_blocks, out_norm_w != nullptr, layout->flags, &plan) != ATTN_RES_OK)
-    return ATTN_RES_EINVAL;
-  if (T * plan.split > INT32_MAX) return ATTN_RES_EINVAL;
-  // no rows: nothing is read or written, so pointers and strides do not matter
-  if (T == 0) return ATTN_RES_OK;
+  return run(kH, prefix, delta, blocks, num_blocks, block_write_idx, res_w, rms_w, out_norm_w,
+             eps, out_eps, out, T, layout, stream);
+}
 
-  const bool has_delta = delta != nullptr;
-  const bool has_onorm = out_norm_w != nullptr;
-  const bool uses_bank = num_blocks > 0 || block_write_idx >= 0;
-  if (!prefix || !res_w || !rms_w || !out || (uses_bank && !blocks)) return ATTN_RES_EINVAL;
-
-  const int64_t pr = layout->prefix_row, dr = layout->delta_row, bt = layout->blocks_token,
-                bs = layout->blocks_slot, orow = layout->out_row;
-  auto bad_row_stride = [](int64_t s) { return s < kH || s > kMaxStride; };
-  if (bad_row_stride(pr) || bad_row_stride(orow) || (has_delta && bad_row_stride(dr)))
-    return ATTN_RES_EINVAL;
-  if (uses_bank) {
-    if (bad_row_stride(bs)) return ATTN_RES_EINVAL;
-    if (T > 1 && (bt < (int64_t)(cap - 1) * bs + kH || bt > kMaxStride)) return ATTN_RES_EINVAL;
-  }
-  if (!aligned16(prefix) || !aligned16(res_w) || !aligned16(rms_w) || !aligned16(out) ||
-      (has_delta && !aligned16(delta)) || (has_onorm && !aligned16(out_norm_w)) ||
-      (uses_bank && !aligned16(blocks)))
-    return ATTN_RES_EALIGN;
-  if ((pr % 8) || (orow % 8) || (has_delta && (dr % 8)) || (uses_bank && ((bs % 8) || (bt % 8))))
-    return ATTN_RES_EALIGN;
-
-  {
-    const int64_t bank_elems = (T - 1) * (T > 1 ? bt : 0) + (int64_t)(cap > 0 ? cap - 1 : 0) * bs + kH;
-    Region regs[7] = {
-        rows_region(prefix, T, pr, true, has_delta),
-        rows_region(delta, T, dr, has_delta, false),
-        Region{reinterpret_cast<uintptr_t>(blocks),
-               reinterpret_cast<uintptr_t>(blocks) + static_cast<uintptr_t>(bank_elems) * 2u,
-               uses_bank, block_write_idx >= 0},
-        rows_region(res_w, 1, kH, true, false),
-        rows_region(rms_w, 1, kH, true, false),
-        rows_region(out_norm_w, 1, kH, has_onorm, false),
-        rows_region(out, T, orow, true, true),
-    };
-    for (int i = 0; i < 7; ++i)
-      for (int j = 0; j < 7; ++j)
-        if (i != j && regs[i].written && overlaps(regs[i], regs[j])) return ATTN_RES_EALIAS;
-  }
-
-  // ---- device and launch ----
-  int dev = 0;
-  attn_res_status_t st = check_device(&dev);
-  if (st != ATTN_RES_OK) return st;
-
-  Params p;
-  p.prefix = prefix;
-  p.delta = delta;
-  p.blocks = blocks;
-  p.res_w = res_w;
-  p.rms_w = rms_w;
-  p.onw = out_norm_w;
-  p.out = out;
-  p.prefix_row = pr;
-  p.delta_row = has_delta ? dr : 0;
-  p.blocks_token = uses_bank ? bt : 0;
-  p.blocks_slot = uses_bank ? bs : 0;
-  p.out_row = orow;
-  p.write_idx = block_write_idx;
-  p.eps = eps;
-  p.out_eps = out_eps;
-  const bool pdl = (layout->flags & ATTN_RES_FLAG_PDL) != 0;
-  cudaError_t e = status_word(dev, &p.err);
-  if (e == cudaSuccess) {
-    if (plan.kernel == ATTN_RES_KERNEL_SPLIT) {
-      LaunchFn fn = lookup(num_blocks, split_index(plan.split), has_delta, has_onorm);
-      if (fn == nullptr) return ATTN_RES_EINVAL;
-      e = fn(p, T, pdl, static_cast<cudaStream_t>(stream), dev);
-    } else {
-      StreamLaunchFn fn = lookup_stream(num_blocks, plan.shape, has_delta, has_onorm);
-      if (fn == nullptr) return ATTN_RES_EINVAL;
-      e = fn(p, T, pdl, static_cast<cudaStream_t>(stream), dev);
-    }
-  }
-  if (e != cudaSuccess) {
-    (void)cudaGetLastError();
-    return ATTN_RES_ECUDA;
-  }
-  return ATTN_RES_OK;
+attn_res_status_t attn_res_h(int64_t H, attn_res_bf16_t* prefix, const attn_res_bf16_t* delta,
+                             attn_res_bf16_t* blocks, int num_blocks, int block_write_idx,
+                             const attn_res_bf16_t* res_w, const attn_res_bf16_t* rms_w,
+                             const attn_res_bf16_t* out_norm_w, float eps, float out_eps,
+                             attn_res_bf16_t* out, int64_t T, const attn_res_layout_t* layout,
+                             void* stream) {
+  return run(H, prefix, delta, blocks, num_blocks, block_write_idx, res_w, rms_w, out_norm_w,
+             eps, out_eps, out, T, layout, stream);
 }
 
 }  // extern "C"

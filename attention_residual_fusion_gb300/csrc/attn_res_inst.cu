@@ -59,4 +59,10 @@ StreamLaunchFn ATTN_RES_CAT(stream_launcher_s, ATTN_RES_S)(int shape_idx, bool d
   }
 }
 
+GenericLaunchFn ATTN_RES_CAT(generic_launcher_s, ATTN_RES_S)(bool d, bool o) {
+  constexpr int S = ATTN_RES_S;
+  if (d) return o ? &launch_generic<S, true, true> : &launch_generic<S, true, false>;
+  return o ? &launch_generic<S, false, true> : &launch_generic<S, false, false>;
+}
+
 }  // namespace attn_res_host

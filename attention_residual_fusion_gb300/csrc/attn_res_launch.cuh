@@ -7,6 +7,7 @@
 
 #include "attn_res_kernel.cuh"
 #include "attn_res_stream.cuh"
+#include "attn_res_generic.cuh"
 
 namespace attn_res_host {
 
@@ -154,6 +155,25 @@ cudaError_t launch_stream(const Params& p, int64_t T, bool pdl, cudaStream_t str
   return cudaLaunchKernelEx(&cfg, kern, p, T);
 }
 
+// The general kernel: one CTA per token row, any H that is a multiple of 8.
+using GenericLaunchFn = cudaError_t (*)(const Params&, int64_t T, int64_t H, bool pdl,
+                                        cudaStream_t stream);
+
+template <int S, bool D, bool O>
+cudaError_t launch_generic(const Params& p, int64_t T, int64_t H, bool pdl, cudaStream_t stream) {
+  void (*kern)(Params, int64_t) = attn_res_dev::attn_res_generic_kernel<S, D, O>;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(T), 1, 1);
+  cfg.blockDim = dim3(attn_res_dev::kGenericThreads, 1, 1);
+  cfg.stream = stream;
+  cfg.attrs = &attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, p, H);
+}
+
 // One row of the table per num_blocks, defined in attn_res_inst.cu (compiled
 // once per S).  Returns nullptr for an unknown split index.
 LaunchFn launcher_s0(int split_idx, bool has_delta, bool has_onorm);
@@ -175,5 +195,15 @@ StreamLaunchFn stream_launcher_s5(int shape_idx, bool d, bool o);
 StreamLaunchFn stream_launcher_s6(int shape_idx, bool d, bool o);
 StreamLaunchFn stream_launcher_s7(int shape_idx, bool d, bool o);
 StreamLaunchFn stream_launcher_s8(int shape_idx, bool d, bool o);
+
+GenericLaunchFn generic_launcher_s0(bool d, bool o);
+GenericLaunchFn generic_launcher_s1(bool d, bool o);
+GenericLaunchFn generic_launcher_s2(bool d, bool o);
+GenericLaunchFn generic_launcher_s3(bool d, bool o);
+GenericLaunchFn generic_launcher_s4(bool d, bool o);
+GenericLaunchFn generic_launcher_s5(bool d, bool o);
+GenericLaunchFn generic_launcher_s6(bool d, bool o);
+GenericLaunchFn generic_launcher_s7(bool d, bool o);
+GenericLaunchFn generic_launcher_s8(bool d, bool o);
 
 }  // namespace attn_res_host

@@ -86,6 +86,7 @@ typedef enum {
 #define ATTN_RES_FLAG_VPT(n) (((uint32_t)(n) & 0xfu) << 24)
 #define ATTN_RES_KERNEL_SPLIT 1
 #define ATTN_RES_KERNEL_STREAM 2
+#define ATTN_RES_KERNEL_GENERIC 3 /* one CTA per row, any H (see attn_res_h) */
 
 /* Memory layout of the tensors, in elements.  A row is H contiguous
  * elements; columns H .. stride-1 are padding that is never read or
@@ -141,6 +142,25 @@ attn_res_status_t attn_res(attn_res_bf16_t* prefix, const attn_res_bf16_t* delta
                            const attn_res_bf16_t* out_norm_w, float eps,
                            float out_eps, attn_res_bf16_t* out, int64_t T,
                            const attn_res_layout_t* layout, void* stream);
+
+/*
+ * attn_res_h -- the same operation for any hidden size H > 0 that is a
+ * multiple of 8 (one 16-byte vector); every [H]- and row-sized argument above
+ * is then H elements wide and strides must be >= H.  H == ATTN_RES_HIDDEN
+ * behaves exactly like attn_res; other widths run a general kernel (one CTA
+ * of 256 threads per token row, same fp32 arithmetic, the rows read three
+ * times through L2) -- a functional path for other model widths, not the
+ * tuned one.  ATTN_RES_FLAG_KERNEL(ATTN_RES_KERNEL_GENERIC) forces that
+ * kernel at H == ATTN_RES_HIDDEN too.  Returns ATTN_RES_EINVAL for a bad H.
+ * (No counterpart on the pages, whose kernel is built for H = 7168 only.)
+ */
+attn_res_status_t attn_res_h(int64_t H, attn_res_bf16_t* prefix,
+                             const attn_res_bf16_t* delta, attn_res_bf16_t* blocks,
+                             int num_blocks, int block_write_idx,
+                             const attn_res_bf16_t* res_w, const attn_res_bf16_t* rms_w,
+                             const attn_res_bf16_t* out_norm_w, float eps, float out_eps,
+                             attn_res_bf16_t* out, int64_t T,
+                             const attn_res_layout_t* layout, void* stream);
 
 /* Static text for a status code. */
 const char* attn_res_status_string(attn_res_status_t status);

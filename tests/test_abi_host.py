@@ -55,10 +55,12 @@ def test_launch_shape(lib):
     assert ls(2, 8, True, ar.FLAG_SPLIT(14))["threads"] == 64
     assert ls(2, 8, True, ar.FLAG_KERNEL(2) | ar.FLAG_SPLIT(4) | ar.FLAG_VPT(2) | ar.FLAG_STAGES(3))["stages"] == 3
     assert ls(9000, 8, True, ar.FLAG_KERNEL(1))["kernel"] == "split"
+    assert ls(10, 8, True, ar.FLAG_KERNEL(3)) == dict(kernel="generic", split=1, stages=0, threads=256, ctas=10, cluster=1)
     assert ls(9000, 8, True, ar.FLAG_SPLIT(7) | ar.FLAG_VPT(2))["threads"] == 64
     assert ls(9000, 8, True, ar.FLAG_SPLIT(7) | ar.FLAG_VPT(1))["threads"] == 128
     for bad in [(-1, 0, 0, 0), (1, 9, 0, 0), (1, -1, 0, 0), (1, 1, 0, ar.FLAG_SPLIT(5)),
-                (1, 1, 0, ar.FLAG_KERNEL(3)), (1, 1, 0, ar.FLAG_KERNEL(2) | ar.FLAG_SPLIT(16)),
+                (1, 1, 0, ar.FLAG_KERNEL(4)), (1, 1, 0, ar.FLAG_KERNEL(2) | ar.FLAG_SPLIT(16)),
+                (1, 1, 0, ar.FLAG_KERNEL(3) | ar.FLAG_SPLIT(7)),
                 (1, 1, 0, ar.FLAG_KERNEL(2) | ar.FLAG_STAGES(4)),
                 (1, 1, 0, ar.FLAG_KERNEL(2) | ar.FLAG_SPLIT(8) | ar.FLAG_VPT(2)),
                 (1, 1, 0, ar.FLAG_KERNEL(2) | ar.FLAG_STAGES(4)),
@@ -173,3 +175,29 @@ def test_optional_pointers(lib):
     assert call(**kw) in (5, 4)  # valid: reaches the device check
     kw["block_write_idx"] = 0
     assert call(**kw) == 1      # a write-back needs a slot
+
+
+def good_h(H, T=4, S=4, cap=8):
+    kw = good(T=T, S=S, cap=cap)
+    lay = kw["layout"]
+    lay.prefix_row = lay.delta_row = lay.out_row = lay.blocks_slot = H
+    lay.blocks_token = cap * H
+    return kw
+
+
+@pytest.mark.parametrize("H,status", [(0, 1), (-8, 1), (4, 1), (12, 1), (7170, 1)])
+def test_other_widths_rejected(lib, H, status):
+    assert ar.call_raw(**good_h(max(H, 8)), H=H) == status
+
+
+def test_other_widths_validate_strides(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a device is present")
+    kw = good_h(64)
+    assert ar.call_raw(**kw, H=64) in (4, 5)        # valid: reaches the device check
+    kw["layout"].prefix_row = 56
+    assert ar.call_raw(**kw, H=64) == 1             # stride below H
+    kw = good_h(64)
+    kw["layout"].flags = ar.FLAG_KERNEL(2)
+    assert ar.call_raw(**kw, H=64) == 1             # only the general kernel takes other widths

@@ -277,3 +277,27 @@ def test_pdl_chain_in_graph(T):
     torch.cuda.synchronize()
     assert np.array_equal(down(d["prefix"]), r["prefix"])
     G.assert_out_close(down(out), r["out"], "pdl-chain")
+
+
+
+# ---- the general kernel (any H, multiple of 8) -----------------------------------
+
+GEN = [(H, S) for H in (8, 16, 64, 200, 1024, 4096) for S in (0, 1, 3, 8)]
+
+
+@pytest.mark.parametrize("H,S", GEN, ids=[f"H{H}_S{S}" for H, S in GEN])
+def test_generic_width_against_oracle(H, S):
+    """Brute force at small and odd widths: every element against the oracle,
+    with delta, output norm and a write-back varying by case."""
+    i = H + S
+    wl = W.make_workload(37, S, capacity=9, has_delta=bool(i & 1), has_out_norm=bool(i & 2),
+                         block_write_idx=[-1, S, 8][i % 3], seed=i, H=H, mixing=True,
+                         slot_stride=H + 8 * (i % 2))
+    full_check(wl, tag=f"generic_H{H}_S{S}")
+
+
+@pytest.mark.parametrize("S", [0, 4, 8])
+def test_generic_kernel_forced_at_full_width(S):
+    wl = W.make_workload(33, S, capacity=9, has_delta=True, has_out_norm=True,
+                         block_write_idx=8, seed=40 + S, mixing=True)
+    full_check(wl, tag=f"generic_forced_S{S}", kernel=ar.KERNEL_GENERIC)
