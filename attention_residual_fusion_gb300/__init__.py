@@ -17,6 +17,7 @@ HIDDEN = 7168
 MAX_BLOCKS = 8
 
 FLAG_PDL = 0x1
+FLAG_TP_GRAM = 0x2
 KERNEL_SPLIT = 1
 KERNEL_STREAM = 2
 KERNEL_GENERIC = 3
@@ -44,7 +45,8 @@ STATUS = {0: "ATTN_RES_OK", 1: "ATTN_RES_EINVAL", 2: "ATTN_RES_EALIGN",
 # Every symbol the header declares.
 EXPORTS = ("attn_res", "attn_res_status_string", "attn_res_hidden_size",
            "attn_res_max_blocks", "attn_res_launch_shape", "attn_res_device_status",
-           "attn_res_selftest_wait_timeout", "attn_res_h")
+           "attn_res_selftest_wait_timeout", "attn_res_h", "attn_res_tp_sums",
+           "attn_res_tp_sq", "attn_res_tp_finish", "attn_res_tp_sums_width")
 
 
 class Layout(ctypes.Structure):
@@ -99,6 +101,17 @@ def lib():
         L.attn_res_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint), ctypes.c_int]
         L.attn_res_selftest_wait_timeout.restype = ctypes.c_int
         L.attn_res_selftest_wait_timeout.argtypes = [ctypes.c_uint, ctypes.POINTER(ctypes.c_uint)]
+        i64, i32, f32 = ctypes.c_int64, ctypes.c_int, ctypes.c_float
+        lp = ctypes.POINTER(Layout)
+        L.attn_res_tp_sums_width.restype = ctypes.c_int
+        L.attn_res_tp_sums_width.argtypes = [i32, i32]
+        L.attn_res_tp_sums.restype = ctypes.c_int
+        L.attn_res_tp_sums.argtypes = [i64, vp, vp, vp, i32, vp, vp, vp, i64, i64, lp, vp]
+        L.attn_res_tp_sq.restype = ctypes.c_int
+        L.attn_res_tp_sq.argtypes = [i64, i64, vp, vp, vp, i32, f32, vp, i64, vp, i64, lp, vp]
+        L.attn_res_tp_finish.restype = ctypes.c_int
+        L.attn_res_tp_finish.argtypes = [i64, i64, vp, vp, vp, i32, i32, vp, f32, f32, vp, i64,
+                                         vp, vp, i64, lp, vp]
         _lib = L
     return _lib
 
@@ -158,6 +171,31 @@ def _ptr(t) -> int:
     return 0 if t is None else int(t.data_ptr())
 
 
+def check_bf16_cuda(**tensors) -> None:
+    import torch
+
+    for name, t in tensors.items():
+        if t is not None and (t.dtype != torch.bfloat16 or t.device.type != "cuda"):
+            raise ValueError(f"{name} must be a CUDA bfloat16 tensor")
+
+
+def make_layout(prefix, delta, blocks, out, flags: int) -> Layout:
+    """attn_res_layout_t from the tensors' strides (row tensors [T, W] and
+    the bank [T, capacity, W], all with unit inner stride; out may be None)."""
+    for name, t in (("prefix", prefix), ("delta", delta), ("out", out)):
+        if t is not None and (t.dim() != 2 or t.stride(1) != 1):
+            raise ValueError(f"{name} must be a [T, H] tensor with unit inner stride")
+    if blocks is not None and (blocks.dim() != 3 or blocks.stride(2) != 1):
+        raise ValueError("blocks must be a [T, capacity, H] tensor with unit inner stride")
+    return Layout(prefix_row=prefix.stride(0),
+                  delta_row=delta.stride(0) if delta is not None else 0,
+                  blocks_token=blocks.stride(0) if blocks is not None else 0,
+                  blocks_slot=blocks.stride(1) if blocks is not None else 0,
+                  out_row=out.stride(0) if out is not None else 0,
+                  blocks_capacity=blocks.shape[1] if blocks is not None else 0,
+                  flags=flags)
+
+
 def attn_res(prefix, delta, blocks, num_blocks: int, block_write_idx: int,
              res_w, rms_w, out_norm_w=None, eps: float = 1e-6,
              out_eps: float = 1e-6, out=None, *, pdl: bool = False,
@@ -173,28 +211,15 @@ def attn_res(prefix, delta, blocks, num_blocks: int, block_write_idx: int,
     """
     import torch
 
-    for name, t in (("prefix", prefix), ("delta", delta), ("blocks", blocks),
-                    ("res_w", res_w), ("rms_w", rms_w), ("out_norm_w", out_norm_w),
-                    ("out", out)):
-        if t is not None and (t.dtype != torch.bfloat16 or t.device.type != "cuda"):
-            raise ValueError(f"{name} must be a CUDA bfloat16 tensor")
+    check_bf16_cuda(prefix=prefix, delta=delta, blocks=blocks, res_w=res_w, rms_w=rms_w,
+                    out_norm_w=out_norm_w, out=out)
     T = prefix.shape[0]
     H = res_w.shape[0]
     if out is None:
         out = torch.empty((T, H), dtype=prefix.dtype, device=prefix.device)
-    for name, t in (("prefix", prefix), ("delta", delta), ("out", out)):
-        if t is not None and (t.dim() != 2 or t.stride(1) != 1):
-            raise ValueError(f"{name} must be a [T, H] tensor with unit inner stride")
-    if blocks is not None and (blocks.dim() != 3 or blocks.stride(2) != 1):
-        raise ValueError("blocks must be a [T, capacity, H] tensor with unit inner stride")
-    lay = Layout(prefix_row=prefix.stride(0),
-                 delta_row=delta.stride(0) if delta is not None else 0,
-                 blocks_token=blocks.stride(0) if blocks is not None else 0,
-                 blocks_slot=blocks.stride(1) if blocks is not None else 0,
-                 out_row=out.stride(0),
-                 blocks_capacity=blocks.shape[1] if blocks is not None else 0,
-                 flags=(FLAG_PDL if pdl else 0) | FLAG_SPLIT(split) |
-                 FLAG_KERNEL(kernel) | FLAG_STAGES(stages) | FLAG_VPT(vpt))
+    lay = make_layout(prefix, delta, blocks, out,
+                      (FLAG_PDL if pdl else 0) | FLAG_SPLIT(split) | FLAG_KERNEL(kernel) |
+                      FLAG_STAGES(stages) | FLAG_VPT(vpt))
     if stream is None:
         stream = torch.cuda.current_stream(prefix.device)
     st = call_raw(_ptr(prefix), _ptr(delta), _ptr(blocks), num_blocks,

@@ -165,6 +165,21 @@ GenericLaunchFn lookup_generic(int S, bool d, bool o) {
   }
 }
 
+TpLaunchFn lookup_tp(int S, int phase, bool d, bool o, bool g) {
+  switch (S) {
+    case 0: return tp_launcher_s0(phase, d, o, g);
+    case 1: return tp_launcher_s1(phase, d, o, g);
+    case 2: return tp_launcher_s2(phase, d, o, g);
+    case 3: return tp_launcher_s3(phase, d, o, g);
+    case 4: return tp_launcher_s4(phase, d, o, g);
+    case 5: return tp_launcher_s5(phase, d, o, g);
+    case 6: return tp_launcher_s6(phase, d, o, g);
+    case 7: return tp_launcher_s7(phase, d, o, g);
+    case 8: return tp_launcher_s8(phase, d, o, g);
+    default: return nullptr;
+  }
+}
+
 StreamLaunchFn lookup_stream(int S, int shape, bool d, bool o) {
   switch (S) {
     case 0: return stream_launcher_s0(shape, d, o);
@@ -210,6 +225,109 @@ LaunchFn lookup(int S, int split_idx, bool d, bool o) {
   }
 }
 
+// The tensor arguments of one call, checked together.
+struct RowArgs {
+  int64_t H = 0;  // width of the rows this call touches
+  int64_t T = 0;
+  const attn_res_layout_t* layout = nullptr;
+  attn_res_bf16_t* prefix = nullptr;
+  const attn_res_bf16_t* delta = nullptr;
+  attn_res_bf16_t* blocks = nullptr;
+  int num_blocks = 0;
+  int write_idx = -1;
+  const attn_res_bf16_t* res_w = nullptr;
+  const attn_res_bf16_t* rms_w = nullptr;
+  const attn_res_bf16_t* onw = nullptr;
+  attn_res_bf16_t* out = nullptr;
+  bool need_weights = true;  // res_w and rms_w are read
+  bool writes = true;        // out, prefix (with delta) and the bank slot are written
+  Region extra[2] = {};      // float buffers of the hidden-sharded calls
+};
+
+// Pointers, strides, alignment and overlaps (pure host checks), then the
+// kernel parameters.  Scalars (num_blocks, write_idx, eps, flags, T >= 0) are
+// checked by the caller first; T must be > 0 here.
+attn_res_status_t check_rows(const RowArgs& a, Params* p) {
+  const int64_t H = a.H, T = a.T;
+  const attn_res_layout_t* L = a.layout;
+  const int cap = L->blocks_capacity;
+  const bool has_delta = a.delta != nullptr;
+  const bool has_onorm = a.onw != nullptr;
+  const bool uses_bank = a.num_blocks > 0 || (a.writes && a.write_idx >= 0);
+  if (!a.prefix || (a.need_weights && (!a.res_w || !a.rms_w)) || (a.writes && !a.out) ||
+      (uses_bank && !a.blocks))
+    return ATTN_RES_EINVAL;
+
+  const int64_t pr = L->prefix_row, dr = L->delta_row, bt = L->blocks_token,
+                bs = L->blocks_slot, orow = L->out_row;
+  auto bad_row_stride = [H](int64_t s) { return s < H || s > kMaxStride; };
+  if (bad_row_stride(pr) || (a.writes && bad_row_stride(orow)) || (has_delta && bad_row_stride(dr)))
+    return ATTN_RES_EINVAL;
+  if (uses_bank) {
+    if (bad_row_stride(bs)) return ATTN_RES_EINVAL;
+    if (T > 1 && (bt < (int64_t)(cap - 1) * bs + H || bt > kMaxStride)) return ATTN_RES_EINVAL;
+  }
+  if (!aligned16(a.prefix) || (a.need_weights && (!aligned16(a.res_w) || !aligned16(a.rms_w))) ||
+      (a.writes && !aligned16(a.out)) || (has_delta && !aligned16(a.delta)) ||
+      (has_onorm && !aligned16(a.onw)) || (uses_bank && !aligned16(a.blocks)))
+    return ATTN_RES_EALIGN;
+  if ((pr % 8) || (a.writes && (orow % 8)) || (has_delta && (dr % 8)) ||
+      (uses_bank && ((bs % 8) || (bt % 8))))
+    return ATTN_RES_EALIGN;
+
+  {
+    const int64_t bank_elems = (T - 1) * (T > 1 ? bt : 0) + (int64_t)(cap > 0 ? cap - 1 : 0) * bs + H;
+    Region regs[9] = {
+        rows_region(a.prefix, T, pr, H, true, a.writes && has_delta),
+        rows_region(a.delta, T, dr, H, has_delta, false),
+        Region{reinterpret_cast<uintptr_t>(a.blocks),
+               reinterpret_cast<uintptr_t>(a.blocks) + static_cast<uintptr_t>(bank_elems) * 2u,
+               uses_bank, a.writes && a.write_idx >= 0},
+        rows_region(a.res_w, 1, H, H, a.need_weights, false),
+        rows_region(a.rms_w, 1, H, H, a.need_weights, false),
+        rows_region(a.onw, 1, H, H, has_onorm, false),
+        rows_region(a.out, T, orow, H, a.writes, a.writes),
+        a.extra[0],
+        a.extra[1],
+    };
+    for (int i = 0; i < 9; ++i)
+      for (int j = 0; j < 9; ++j)
+        if (i != j && regs[i].written && overlaps(regs[i], regs[j])) return ATTN_RES_EALIAS;
+  }
+
+  p->prefix = a.prefix;
+  p->delta = a.delta;
+  p->blocks = a.blocks;
+  p->res_w = a.res_w;
+  p->rms_w = a.rms_w;
+  p->onw = a.onw;
+  p->out = a.out;
+  p->prefix_row = pr;
+  p->delta_row = has_delta ? dr : 0;
+  p->blocks_token = uses_bank ? bt : 0;
+  p->blocks_slot = uses_bank ? bs : 0;
+  p->out_row = a.writes ? orow : 0;
+  p->write_idx = a.writes ? a.write_idx : -1;
+  p->err = nullptr;
+  return ATTN_RES_OK;
+}
+
+// Scalars every entry point checks the same way.
+attn_res_status_t check_scalars(int64_t T, int64_t H, int num_blocks, int write_idx, float eps,
+                                float out_eps, const attn_res_layout_t* layout,
+                                uint32_t known = kKnownFlags) {
+  if (layout == nullptr || T < 0) return ATTN_RES_EINVAL;
+  if (H <= 0 || H % 8 != 0 || H > kMaxStride) return ATTN_RES_EINVAL;
+  const int cap = layout->blocks_capacity;
+  if (num_blocks < 0 || num_blocks > ATTN_RES_MAX_BLOCKS || cap < 0 || num_blocks > cap)
+    return ATTN_RES_EINVAL;
+  if (write_idx < -1 || write_idx >= cap) return ATTN_RES_EINVAL;
+  if (!std::isfinite(eps) || eps < 0.f || !std::isfinite(out_eps) || out_eps < 0.f)
+    return ATTN_RES_EINVAL;
+  if ((layout->flags & ~known) != 0) return ATTN_RES_EINVAL;
+  return ATTN_RES_OK;
+}
+
 attn_res_status_t run(int64_t H, attn_res_bf16_t* prefix, const attn_res_bf16_t* delta,
                       attn_res_bf16_t* blocks, int num_blocks, int block_write_idx,
                       const attn_res_bf16_t* res_w, const attn_res_bf16_t* rms_w,
@@ -217,15 +335,9 @@ attn_res_status_t run(int64_t H, attn_res_bf16_t* prefix, const attn_res_bf16_t*
                       attn_res_bf16_t* out, int64_t T, const attn_res_layout_t* layout,
                       void* stream) {
   // ---- arguments (pure host checks, no CUDA call) ----
-  if (layout == nullptr || T < 0) return ATTN_RES_EINVAL;
-  if (H <= 0 || H % 8 != 0 || H > kMaxStride) return ATTN_RES_EINVAL;
-  const int cap = layout->blocks_capacity;
-  if (num_blocks < 0 || num_blocks > ATTN_RES_MAX_BLOCKS || cap < 0 || num_blocks > cap)
-    return ATTN_RES_EINVAL;
-  if (block_write_idx < -1 || block_write_idx >= cap) return ATTN_RES_EINVAL;
-  if (!std::isfinite(eps) || eps < 0.f || !std::isfinite(out_eps) || out_eps < 0.f)
-    return ATTN_RES_EINVAL;
-  if ((layout->flags & ~kKnownFlags) != 0) return ATTN_RES_EINVAL;
+  attn_res_status_t st =
+      check_scalars(T, H, num_blocks, block_write_idx, eps, out_eps, layout);
+  if (st != ATTN_RES_OK) return st;
   Plan plan;
   if (make_plan(T, num_blocks, out_norm_w != nullptr, layout->flags, &plan) != ATTN_RES_OK)
     return ATTN_RES_EINVAL;
@@ -241,66 +353,31 @@ attn_res_status_t run(int64_t H, attn_res_bf16_t* prefix, const attn_res_bf16_t*
   // no rows: nothing is read or written, so pointers and strides do not matter
   if (T == 0) return ATTN_RES_OK;
 
+  RowArgs a;
+  a.H = H;
+  a.T = T;
+  a.layout = layout;
+  a.prefix = prefix;
+  a.delta = delta;
+  a.blocks = blocks;
+  a.num_blocks = num_blocks;
+  a.write_idx = block_write_idx;
+  a.res_w = res_w;
+  a.rms_w = rms_w;
+  a.onw = out_norm_w;
+  a.out = out;
+  Params p;
+  st = check_rows(a, &p);
+  if (st != ATTN_RES_OK) return st;
   const bool has_delta = delta != nullptr;
   const bool has_onorm = out_norm_w != nullptr;
-  const bool uses_bank = num_blocks > 0 || block_write_idx >= 0;
-  if (!prefix || !res_w || !rms_w || !out || (uses_bank && !blocks)) return ATTN_RES_EINVAL;
-
-  const int64_t pr = layout->prefix_row, dr = layout->delta_row, bt = layout->blocks_token,
-                bs = layout->blocks_slot, orow = layout->out_row;
-  auto bad_row_stride = [H](int64_t s) { return s < H || s > kMaxStride; };
-  if (bad_row_stride(pr) || bad_row_stride(orow) || (has_delta && bad_row_stride(dr)))
-    return ATTN_RES_EINVAL;
-  if (uses_bank) {
-    if (bad_row_stride(bs)) return ATTN_RES_EINVAL;
-    if (T > 1 && (bt < (int64_t)(cap - 1) * bs + H || bt > kMaxStride)) return ATTN_RES_EINVAL;
-  }
-  if (!aligned16(prefix) || !aligned16(res_w) || !aligned16(rms_w) || !aligned16(out) ||
-      (has_delta && !aligned16(delta)) || (has_onorm && !aligned16(out_norm_w)) ||
-      (uses_bank && !aligned16(blocks)))
-    return ATTN_RES_EALIGN;
-  if ((pr % 8) || (orow % 8) || (has_delta && (dr % 8)) || (uses_bank && ((bs % 8) || (bt % 8))))
-    return ATTN_RES_EALIGN;
-
-  {
-    const int64_t bank_elems = (T - 1) * (T > 1 ? bt : 0) + (int64_t)(cap > 0 ? cap - 1 : 0) * bs + H;
-    Region regs[7] = {
-        rows_region(prefix, T, pr, H, true, has_delta),
-        rows_region(delta, T, dr, H, has_delta, false),
-        Region{reinterpret_cast<uintptr_t>(blocks),
-               reinterpret_cast<uintptr_t>(blocks) + static_cast<uintptr_t>(bank_elems) * 2u,
-               uses_bank, block_write_idx >= 0},
-        rows_region(res_w, 1, H, H, true, false),
-        rows_region(rms_w, 1, H, H, true, false),
-        rows_region(out_norm_w, 1, H, H, has_onorm, false),
-        rows_region(out, T, orow, H, true, true),
-    };
-    for (int i = 0; i < 7; ++i)
-      for (int j = 0; j < 7; ++j)
-        if (i != j && regs[i].written && overlaps(regs[i], regs[j])) return ATTN_RES_EALIAS;
-  }
+  p.eps = eps;
+  p.out_eps = out_eps;
 
   // ---- device and launch ----
   int dev = 0;
-  attn_res_status_t st = check_device(&dev);
+  st = check_device(&dev);
   if (st != ATTN_RES_OK) return st;
-
-  Params p;
-  p.prefix = prefix;
-  p.delta = delta;
-  p.blocks = blocks;
-  p.res_w = res_w;
-  p.rms_w = rms_w;
-  p.onw = out_norm_w;
-  p.out = out;
-  p.prefix_row = pr;
-  p.delta_row = has_delta ? dr : 0;
-  p.blocks_token = uses_bank ? bt : 0;
-  p.blocks_slot = uses_bank ? bs : 0;
-  p.out_row = orow;
-  p.write_idx = block_write_idx;
-  p.eps = eps;
-  p.out_eps = out_eps;
   const bool pdl = (layout->flags & ATTN_RES_FLAG_PDL) != 0;
   cudaError_t e = status_word(dev, &p.err);
   if (e == cudaSuccess) {
@@ -325,9 +402,136 @@ attn_res_status_t run(int64_t H, attn_res_bf16_t* prefix, const attn_res_bf16_t*
   return ATTN_RES_OK;
 }
 
+Region floats_region(const void* p, int64_t T, int64_t row, int64_t width, bool written) {
+  Region r{0, 0, p != nullptr, written};
+  if (r.used) {
+    r.lo = reinterpret_cast<uintptr_t>(p);
+    r.hi = r.lo + static_cast<uintptr_t>((T - 1) * row + width) * 4u;
+  }
+  return r;
+}
+
+// Threads per CTA of the sharded kernels: one 16-byte vector per thread where
+// the shard fits in 256 threads, in whole warps.
+int tp_threads(int64_t Hs) {
+  const int64_t nv = Hs / 8;
+  return static_cast<int>(nv >= attn_res_dev::kTpMaxThreads ? attn_res_dev::kTpMaxThreads
+                                                            : ((nv + 31) / 32) * 32);
+}
+
+// One phase of the hidden-sharded mixture: shared checks and launch.
+// phase 0 reads the rows and weights and writes sums; phase 1 reads the rows
+// and sums and writes sq; phase 2 reads the rows, sums and (with an output
+// norm) sq, and writes out and the write-backs of c.
+attn_res_status_t run_tp(int phase, int64_t Hs, int64_t H, attn_res_bf16_t* prefix,
+                         const attn_res_bf16_t* delta, attn_res_bf16_t* blocks, int num_blocks,
+                         int block_write_idx, const attn_res_bf16_t* res_w,
+                         const attn_res_bf16_t* rms_w, bool onorm,
+                         const attn_res_bf16_t* out_norm_w, float eps, float out_eps, float* sums,
+                         int64_t sums_row, float* sq, attn_res_bf16_t* out, int64_t T,
+                         const attn_res_layout_t* layout, void* stream) {
+  // the sharded kernels have one launch shape: only PDL and TP_GRAM apply
+  attn_res_status_t st = check_scalars(T, Hs, num_blocks, block_write_idx, eps, out_eps, layout,
+                                       ATTN_RES_FLAG_PDL | ATTN_RES_FLAG_TP_GRAM);
+  if (st != ATTN_RES_OK) return st;
+  const bool gram = (layout->flags & ATTN_RES_FLAG_TP_GRAM) != 0;
+  if (phase == 1 && gram) return ATTN_RES_EINVAL;  // the Gram form has no sq phase
+  const int nr = attn_res_tp_sums_width(num_blocks, gram ? 1 : 0);
+  if (H < Hs || H > kMaxStride || sums_row < nr || sums_row > kMaxStride) return ATTN_RES_EINVAL;
+  if (T > INT32_MAX) return ATTN_RES_EINVAL;
+  if (T == 0) return ATTN_RES_OK;
+  const bool uses_sq = phase >= 1 && onorm && !gram;
+  if (sums == nullptr || (uses_sq && sq == nullptr)) return ATTN_RES_EINVAL;
+  if ((reinterpret_cast<uintptr_t>(sums) & 3u) || (uses_sq && (reinterpret_cast<uintptr_t>(sq) & 3u)))
+    return ATTN_RES_EALIGN;
+
+  RowArgs a;
+  a.H = Hs;
+  a.T = T;
+  a.layout = layout;
+  a.prefix = prefix;
+  a.delta = delta;
+  a.blocks = blocks;
+  a.num_blocks = num_blocks;
+  a.write_idx = block_write_idx;
+  a.res_w = res_w;
+  a.rms_w = rms_w;
+  a.onw = phase == 2 ? out_norm_w : nullptr;
+  a.out = out;
+  a.need_weights = phase == 0;
+  a.writes = phase == 2;
+  a.extra[0] = floats_region(sums, T, sums_row, nr, phase == 0);
+  a.extra[1] = floats_region(uses_sq ? sq : nullptr, T, 1, 1, phase == 1);
+  Params p;
+  st = check_rows(a, &p);
+  if (st != ATTN_RES_OK) return st;
+  p.eps = eps;
+  p.out_eps = out_eps;
+  int dev = 0;
+  st = check_device(&dev);
+  if (st != ATTN_RES_OK) return st;
+  TpArgs ta;
+  ta.Hs = Hs;
+  ta.inv_h = 1.0f / static_cast<float>(H);
+  ta.sums = sums;
+  ta.sums_row = sums_row;
+  ta.sq = uses_sq ? sq : nullptr;
+  TpLaunchFn fn = lookup_tp(num_blocks, phase, delta != nullptr, onorm, gram);
+  if (fn == nullptr) return ATTN_RES_EINVAL;
+  const int threads = tp_threads(Hs);
+  cudaError_t e = status_word(dev, &p.err);
+  if (e == cudaSuccess)
+    e = fn(p, ta, T, threads, (layout->flags & ATTN_RES_FLAG_PDL) != 0,
+           static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) {
+    (void)cudaGetLastError();
+    return ATTN_RES_ECUDA;
+  }
+  return ATTN_RES_OK;
+}
+
 }  // namespace
 
 extern "C" {
+
+attn_res_status_t attn_res_tp_sums(int64_t Hs, const attn_res_bf16_t* prefix,
+                                   const attn_res_bf16_t* delta, const attn_res_bf16_t* blocks,
+                                   int num_blocks, const attn_res_bf16_t* res_w,
+                                   const attn_res_bf16_t* rms_w, float* sums, int64_t sums_row,
+                                   int64_t T, const attn_res_layout_t* layout, void* stream) {
+  return run_tp(0, Hs, Hs, const_cast<attn_res_bf16_t*>(prefix), delta,
+                const_cast<attn_res_bf16_t*>(blocks), num_blocks, -1, res_w, rms_w, false,
+                nullptr, 0.f, 0.f, sums, sums_row, nullptr, nullptr, T, layout, stream);
+}
+
+attn_res_status_t attn_res_tp_sq(int64_t Hs, int64_t H, const attn_res_bf16_t* prefix,
+                                 const attn_res_bf16_t* delta, const attn_res_bf16_t* blocks,
+                                 int num_blocks, float eps, const float* sums, int64_t sums_row,
+                                 float* sq, int64_t T, const attn_res_layout_t* layout,
+                                 void* stream) {
+  return run_tp(1, Hs, H, const_cast<attn_res_bf16_t*>(prefix), delta,
+                const_cast<attn_res_bf16_t*>(blocks), num_blocks, -1, nullptr, nullptr, true,
+                nullptr, eps, 0.f, const_cast<float*>(sums), sums_row, sq, nullptr, T, layout,
+                stream);
+}
+
+attn_res_status_t attn_res_tp_finish(int64_t Hs, int64_t H, attn_res_bf16_t* prefix,
+                                     const attn_res_bf16_t* delta, attn_res_bf16_t* blocks,
+                                     int num_blocks, int block_write_idx,
+                                     const attn_res_bf16_t* out_norm_w, float eps, float out_eps,
+                                     const float* sums, int64_t sums_row, const float* sq,
+                                     attn_res_bf16_t* out, int64_t T,
+                                     const attn_res_layout_t* layout, void* stream) {
+  return run_tp(2, Hs, H, prefix, delta, blocks, num_blocks, block_write_idx, nullptr, nullptr,
+                out_norm_w != nullptr, out_norm_w, eps, out_eps, const_cast<float*>(sums),
+                sums_row, const_cast<float*>(sq), out, T, layout, stream);
+}
+
+int attn_res_tp_sums_width(int num_blocks, int gram) {
+  if (num_blocks < 0 || num_blocks > ATTN_RES_MAX_BLOCKS) return -1;
+  const int n = num_blocks + 1;
+  return 2 * n + (gram ? n * (n - 1) / 2 : 0);
+}
 
 const char* attn_res_status_string(attn_res_status_t s) {
   switch (s) {

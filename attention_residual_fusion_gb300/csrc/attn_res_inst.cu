@@ -65,4 +65,22 @@ GenericLaunchFn ATTN_RES_CAT(generic_launcher_s, ATTN_RES_S)(bool d, bool o) {
   return o ? &launch_generic<S, false, true> : &launch_generic<S, false, false>;
 }
 
+template <int S, bool D>
+TpLaunchFn tp_finish_fn(bool o, bool g) {
+  if (o) return g ? &launch_tp_finish<S, D, true, true> : &launch_tp_finish<S, D, true, false>;
+  return &launch_tp_finish<S, D, false, false>;  // without an output norm GRAM changes nothing
+}
+
+TpLaunchFn ATTN_RES_CAT(tp_launcher_s, ATTN_RES_S)(int phase, bool d, bool o, bool g) {
+  constexpr int S = ATTN_RES_S;
+  switch (phase) {
+    case 0:
+      if (d) return g ? &launch_tp_sums<S, true, true> : &launch_tp_sums<S, true, false>;
+      return g ? &launch_tp_sums<S, false, true> : &launch_tp_sums<S, false, false>;
+    case 1: return d ? &launch_tp_sq<S, true> : &launch_tp_sq<S, false>;
+    case 2: return d ? tp_finish_fn<S, true>(o, g) : tp_finish_fn<S, false>(o, g);
+    default: return nullptr;
+  }
+}
+
 }  // namespace attn_res_host

@@ -8,6 +8,7 @@
 #include "attn_res_kernel.cuh"
 #include "attn_res_stream.cuh"
 #include "attn_res_generic.cuh"
+#include "attn_res_tp.cuh"
 
 namespace attn_res_host {
 
@@ -174,6 +175,41 @@ cudaError_t launch_generic(const Params& p, int64_t T, int64_t H, bool pdl, cuda
   return cudaLaunchKernelEx(&cfg, kern, p, H);
 }
 
+// Hidden-sharded phases: one CTA per token row, `threads` (32..256) wide.
+using attn_res_dev::TpArgs;
+using TpLaunchFn = cudaError_t (*)(const Params&, const TpArgs&, int64_t T, int threads, bool pdl,
+                                   cudaStream_t stream);
+
+template <class Kern>
+cudaError_t launch_tp(Kern kern, const Params& p, const TpArgs& a, int64_t T, int threads,
+                      bool pdl, cudaStream_t stream) {
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(T), 1, 1);
+  cfg.blockDim = dim3(static_cast<unsigned>(threads), 1, 1);
+  cfg.stream = stream;
+  cfg.attrs = &attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, p, a);
+}
+template <int S, bool D, bool G>
+cudaError_t launch_tp_sums(const Params& p, const TpArgs& a, int64_t T, int th, bool pdl,
+                           cudaStream_t s) {
+  return launch_tp(attn_res_dev::attn_res_tp_sums_kernel<S, D, G>, p, a, T, th, pdl, s);
+}
+template <int S, bool D>
+cudaError_t launch_tp_sq(const Params& p, const TpArgs& a, int64_t T, int th, bool pdl,
+                         cudaStream_t s) {
+  return launch_tp(attn_res_dev::attn_res_tp_sq_kernel<S, D>, p, a, T, th, pdl, s);
+}
+template <int S, bool D, bool O, bool G>
+cudaError_t launch_tp_finish(const Params& p, const TpArgs& a, int64_t T, int th, bool pdl,
+                             cudaStream_t s) {
+  return launch_tp(attn_res_dev::attn_res_tp_finish_kernel<S, D, O, G>, p, a, T, th, pdl, s);
+}
+
 // One row of the table per num_blocks, defined in attn_res_inst.cu (compiled
 // once per S).  Returns nullptr for an unknown split index.
 LaunchFn launcher_s0(int split_idx, bool has_delta, bool has_onorm);
@@ -205,5 +241,16 @@ GenericLaunchFn generic_launcher_s5(bool d, bool o);
 GenericLaunchFn generic_launcher_s6(bool d, bool o);
 GenericLaunchFn generic_launcher_s7(bool d, bool o);
 GenericLaunchFn generic_launcher_s8(bool d, bool o);
+
+// phase 0: sums, 1: sum of squares, 2: finish
+TpLaunchFn tp_launcher_s0(int phase, bool d, bool o, bool g);
+TpLaunchFn tp_launcher_s1(int phase, bool d, bool o, bool g);
+TpLaunchFn tp_launcher_s2(int phase, bool d, bool o, bool g);
+TpLaunchFn tp_launcher_s3(int phase, bool d, bool o, bool g);
+TpLaunchFn tp_launcher_s4(int phase, bool d, bool o, bool g);
+TpLaunchFn tp_launcher_s5(int phase, bool d, bool o, bool g);
+TpLaunchFn tp_launcher_s6(int phase, bool d, bool o, bool g);
+TpLaunchFn tp_launcher_s7(int phase, bool d, bool o, bool g);
+TpLaunchFn tp_launcher_s8(int phase, bool d, bool o, bool g);
 
 }  // namespace attn_res_host

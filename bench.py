@@ -20,6 +20,8 @@ than L2, so no flush is needed between steps.
              dependent launch (T=1 and T=1024)
   prefill_cells  T=1024/2048 prefill cells: µs per call from CUDA-graph
              replay, cycling through input copies larger than 3x L2
+  tp_cells   one rank's kernels of the hidden-sharded (TP8) mixture, both
+             exchange forms, all-reduces excluded
   cpu_baseline  the CPU oracle on a bounded sample of the same workload
 
 ``--impl reference`` times the CPU oracle on the same workload and metric.
@@ -307,6 +309,67 @@ def sweep_prefill(ar, torch, dev, stream, peak):
     return rows
 
 
+def tp_cells(ar, torch, dev, stream, peak, ranks=8):
+    """One rank's kernels of the hidden-sharded mixture (shard width H/8, the
+    TP8 layout): µs per step from CUDA-graph replay, contiguous [T, H/8]
+    shard tensors, input copies rotated over more than 3x L2.  The
+    all-reduces between the kernels are not part of the number (one GPU:
+    there is nothing to exchange with); `kernels` says how many launches a
+    step makes.  `frac` = single-pass algorithmic bytes of the shard per
+    step / time, against the measured copy bandwidth."""
+    from attention_residual_fusion_gb300 import tp
+    rows = []
+    for name in ("long_prefill", "single_token"):
+        wl, _ = make(name)
+        Hs = wl.H // ranks
+        full = device_tensors(wl, torch, dev)
+        shard = {k: (None if v is None else
+                     (v[:, :, :Hs] if k == "bank" else v[..., :Hs]).contiguous())
+                 for k, v in full.items()}
+        del full
+        alg = wl.algorithmic_bytes() * Hs // wl.H
+        l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+        n = min(16, max(1, -(-3 * l2 // alg)))
+        sets = [shard] + [{k: (v.clone() if v is not None and k in ("prefix", "delta", "bank", "out")
+                               else v) for k, v in shard.items()} for _ in range(n - 1)]
+        for gram in (False, True):
+            def step(st):
+                tp.attn_res_tp(st["prefix"], st["delta"], st["bank"], wl.num_blocks,
+                               wl.block_write_idx, st["res"], st["rms"], st["onw"], wl.eps,
+                               wl.out_eps, st["out"], H=wl.H, all_reduce=lambda x: None,
+                               gram=gram, stream=stream)
+            calls = 16 if wl.T > 1 else 64
+            with torch.cuda.stream(stream):
+                for st in sets:
+                    step(st)
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for i in range(calls):
+                    step(sets[i % len(sets)])
+            g.replay()
+            torch.cuda.synchronize()
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(stream):
+                a.record(stream)
+                g.replay()
+                b.record(stream)
+            torch.cuda.synchronize()
+            del g
+            us = a.elapsed_time(b) * 1e3 / calls
+            gbs = alg / (us * 1e-6) / 1e9
+            rows.append({"workload": f"{name} shard 1/{ranks} (H_s={Hs})",
+                         "form": "single exchange (Gram)" if gram else "two exchanges",
+                         "kernels": 2 if gram else 3, "all_reduces": 1 if gram else 2,
+                         "us_per_step": round(us, 3), "tokens_per_s": round(wl.T / (us * 1e-6), 1),
+                         "gbs": round(gbs, 1), "frac": round(gbs / peak, 4),
+                         "input_sets": len(sets)})
+        del sets, shard
+        torch.cuda.empty_cache()
+    return rows
+
+
 def pdl_chain(ar, torch, dev, stream):
     """Back-to-back calls replayed from a CUDA graph, with and without
     programmatic dependent launch (each call's bank-row and weight loads may
@@ -510,6 +573,10 @@ def run_ours(args, rank, world, local_rank, dist):
         torch.cuda.empty_cache()
         line["prefill_cells"] = sweep_prefill(ar, torch, dev, stream, peak)
         t = None
+    if rank == 0 and not args.no_tp:
+        t = None
+        torch.cuda.empty_cache()
+        line["tp_cells"] = tp_cells(ar, torch, dev, stream, peak)
     if not args.no_e2e:
         t = None
         torch.cuda.empty_cache()
@@ -581,6 +648,7 @@ def main():
     ap.add_argument("--no-latency", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-sweep", action="store_true", help="skip the prefill T=1024/2048 cells")
+    ap.add_argument("--no-tp", action="store_true", help="skip the hidden-sharded cells")
     args = ap.parse_args()
 
     world = int(os.environ.get("WORLD_SIZE", "1"))

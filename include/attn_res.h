@@ -65,6 +65,10 @@ typedef enum {
  * the wait: PDL discipline in the key source excerpts of vllm PR #54261. */
 #define ATTN_RES_FLAG_PDL 0x1u
 
+/* Hidden-sharded calls only (attn_res_tp_*; attn_res and attn_res_h reject
+ * it): the single-exchange form, see attn_res_tp_sums below. */
+#define ATTN_RES_FLAG_TP_GRAM 0x2u
+
 /* Tuning overrides (0 = automatic).  Results do not depend on them beyond
  * fp32 summation order.
  *   SPLIT(k):  CTAs (one thread-block cluster) a token row is split over;
@@ -161,6 +165,77 @@ attn_res_status_t attn_res_h(int64_t H, attn_res_bf16_t* prefix,
                              const attn_res_bf16_t* out_norm_w, float eps, float out_eps,
                              attn_res_bf16_t* out, int64_t T,
                              const attn_res_layout_t* layout, void* stream);
+
+/*
+ * Hidden-sharded (tensor-parallel) mixture.  The Kimi-K3 deployments the
+ * prhub summary of vllm PR #54261 evaluates (impact section: TP8, TEP8,
+ * DEP16, ...) may hold a column shard of each row per rank.  The logits need
+ * full-row sums and the output norm a full-row sum of squares, so the
+ * operation above splits at those two points; the caller all-reduces (sums)
+ * the small float buffers between the calls:
+ *
+ *   attn_res_tp_sums   -> all-reduce sums [T, 2N]   (N = num_blocks + 1)
+ *   attn_res_tp_sq     -> all-reduce sq [T]         (output norm only)
+ *   attn_res_tp_finish
+ *
+ * Each rank passes its own shard: every row-sized argument (prefix, delta,
+ * blocks rows, res_w, rms_w, out_norm_w, out) is the Hs columns that rank
+ * owns, with the strides and layout rules of attn_res_h for width Hs (a
+ * multiple of 8); H is the full hidden size (the sum of the shard widths),
+ * used in mean(x^2) and mean(acc^2).  With one rank (Hs == H) the three calls
+ * compute the same result as attn_res_h.  Float buffers are fp32 device
+ * memory owned by the caller, 4-byte aligned; sums has sums_row >=
+ * attn_res_tp_sums_width(num_blocks, gram) floats between token rows:
+ * entries 0..N-1 are sum(x_i^2), N..2N-1 are <x_i, q> over the shard
+ * (x_S = c).  layout->flags accepts ATTN_RES_FLAG_PDL and
+ * ATTN_RES_FLAG_TP_GRAM only.  One CTA of 32..256 threads per token row.
+ * Errors as for attn_res (nothing is launched unless ATTN_RES_OK is
+ * returned); a written float buffer that overlaps any other argument is
+ * ATTN_RES_EALIAS.
+ *
+ * Single exchange (ATTN_RES_FLAG_TP_GRAM set on attn_res_tp_sums and
+ * attn_res_tp_finish): attn_res_tp_sums also writes g_ij = <x_i, x_j> over
+ * the shard for i < j (entries 2N.., row-major over i), and
+ * attn_res_tp_finish takes sum(acc^2) = sum_i w_i^2 ss_i + 2 sum_{i<j} w_i
+ * w_j g_ij from the reduced entries: one all-reduce and no attn_res_tp_sq
+ * call (which rejects the flag).  Exact in real arithmetic; in fp32 the
+ * output norm loses relative accuracy where the weighted rows cancel
+ * (|acc| << sum_i w_i |x_i|), so the default is the two-exchange form.
+ */
+
+/* Floats per token row of `sums`: 2N, plus N(N-1)/2 with gram != 0
+ * (N = num_blocks + 1); -1 for num_blocks outside 0..8. */
+int attn_res_tp_sums_width(int num_blocks, int gram);
+
+/* Per-shard sums; reads prefix, delta, blocks[t, 0..num_blocks), res_w,
+ * rms_w; writes sums[t, 0..attn_res_tp_sums_width(num_blocks, gram)). */
+attn_res_status_t attn_res_tp_sums(int64_t Hs, const attn_res_bf16_t* prefix,
+                                   const attn_res_bf16_t* delta, const attn_res_bf16_t* blocks,
+                                   int num_blocks, const attn_res_bf16_t* res_w,
+                                   const attn_res_bf16_t* rms_w, float* sums, int64_t sums_row,
+                                   int64_t T, const attn_res_layout_t* layout, void* stream);
+
+/* Output-norm partial: softmax from the reduced sums, acc over the shard,
+ * sq[t] = sum(acc^2) over the shard.  Reads prefix, delta, blocks, sums;
+ * writes sq[0..T).  sq must not be NULL. */
+attn_res_status_t attn_res_tp_sq(int64_t Hs, int64_t H, const attn_res_bf16_t* prefix,
+                                 const attn_res_bf16_t* delta, const attn_res_bf16_t* blocks,
+                                 int num_blocks, float eps, const float* sums, int64_t sums_row,
+                                 float* sq, int64_t T, const attn_res_layout_t* layout,
+                                 void* stream);
+
+/* Output and write-backs of the shard: softmax from the reduced sums, acc,
+ * out (normalised with the reduced sq, or with the Gram entries under
+ * ATTN_RES_FLAG_TP_GRAM, when out_norm_w != NULL; sq may be NULL otherwise),
+ * prefix[t] = c when delta != NULL, blocks[t, block_write_idx] = c when
+ * block_write_idx >= 0. */
+attn_res_status_t attn_res_tp_finish(int64_t Hs, int64_t H, attn_res_bf16_t* prefix,
+                                     const attn_res_bf16_t* delta, attn_res_bf16_t* blocks,
+                                     int num_blocks, int block_write_idx,
+                                     const attn_res_bf16_t* out_norm_w, float eps, float out_eps,
+                                     const float* sums, int64_t sums_row, const float* sq,
+                                     attn_res_bf16_t* out, int64_t T,
+                                     const attn_res_layout_t* layout, void* stream);
 
 /* Static text for a status code. */
 const char* attn_res_status_string(attn_res_status_t status);

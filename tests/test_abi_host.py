@@ -66,7 +66,8 @@ def test_launch_shape(lib):
                 (1, 1, 0, ar.FLAG_KERNEL(2) | ar.FLAG_STAGES(4)),
                 (1, 1, 0, ar.FLAG_KERNEL(2) | ar.FLAG_SPLIT(7) | ar.FLAG_VPT(1) | ar.FLAG_STAGES(3)),
                 (1, 1, 0, ar.FLAG_KERNEL(1) | ar.FLAG_VPT(2)),
-                (1, 1, 0, ar.FLAG_KERNEL(1) | ar.FLAG_STAGES(2)), (1, 1, 0, 1 << 30)]:
+                (1, 1, 0, ar.FLAG_KERNEL(1) | ar.FLAG_STAGES(2)), (1, 1, 0, 1 << 30),
+                (1, 1, 0, ar.FLAG_TP_GRAM)]:
         with pytest.raises(ar.AttnResError):
             ls(*bad)
 
@@ -154,7 +155,7 @@ def test_append_slot_equal_to_capacity_is_rejected(lib):
     ("prefix_row", H - 8, 1), ("out_row", 100, 1), ("delta_row", 0, 1),
     ("blocks_slot", H - 8, 1), ("blocks_token", 7 * H, 1),
     ("prefix_row", H + 4, 2), ("blocks_slot", 7232 + 4, 2), ("out_row", H + 1, 2),
-    ("blocks_capacity", -1, 1), ("flags", 0x4, 1), ("flags", ar.FLAG_SPLIT(5), 1),
+    ("blocks_capacity", -1, 1), ("flags", 0x4, 1), ("flags", ar.FLAG_TP_GRAM, 1), ("flags", ar.FLAG_SPLIT(5), 1),
     ("flags", ar.FLAG_KERNEL(7), 1), ("flags", ar.FLAG_KERNEL(2) | ar.FLAG_SPLIT(16), 1),
 ])
 def test_layout_rejections(lib, field, value, status):
@@ -201,3 +202,111 @@ def test_other_widths_validate_strides(lib):
     kw = good_h(64)
     kw["layout"].flags = ar.FLAG_KERNEL(2)
     assert ar.call_raw(**kw, H=64) == 1             # only the general kernel takes other widths
+
+
+# ---- hidden-sharded entry points (host checks only) ----
+
+HS = 896  # one rank's shard of 7168 over 8 ranks
+
+
+def tp_layout(T=4, cap=8, flags=0, W=HS):
+    return ar.Layout(prefix_row=W, delta_row=W, blocks_token=cap * W, blocks_slot=W,
+                     out_row=W, blocks_capacity=cap, flags=flags)
+
+
+def tp_call(phase, T=4, S=4, Hs=HS, Hfull=H, sums_row=None, sums=None, sq=None, widx=-1,
+            onorm=True, flags=0, **ptrs):
+    import ctypes
+
+    L = ar.lib()
+    lay = tp_layout(T=T, flags=flags)
+    p = dict(prefix=addr(0), delta=addr(1), blocks=addr(2), res_w=addr(3), rms_w=addr(4),
+             onw=addr(5) if onorm else 0, out=addr(6))
+    p.update(ptrs)
+    sums = addr(7) if sums is None else sums
+    sq = addr(8) if sq is None else sq
+    sums_row = 2 * (S + 1) if sums_row is None else sums_row
+    n = lambda v: v or None  # noqa: E731
+    if phase == 0:
+        return L.attn_res_tp_sums(Hs, n(p["prefix"]), n(p["delta"]), n(p["blocks"]), S,
+                                  n(p["res_w"]), n(p["rms_w"]), n(sums), sums_row, T,
+                                  ctypes.byref(lay), None)
+    if phase == 1:
+        return L.attn_res_tp_sq(Hs, Hfull, n(p["prefix"]), n(p["delta"]), n(p["blocks"]), S,
+                                1e-6, n(sums), sums_row, n(sq), T, ctypes.byref(lay), None)
+    return L.attn_res_tp_finish(Hs, Hfull, n(p["prefix"]), n(p["delta"]), n(p["blocks"]), S,
+                                widx, n(p["onw"]), 1e-6, 1e-6, n(sums), sums_row, n(sq),
+                                n(p["out"]), T, ctypes.byref(lay), None)
+
+
+@pytest.mark.parametrize("phase", [0, 1, 2])
+def test_tp_valid_arguments_reach_the_device_check(lib, phase):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a device is present")
+    assert tp_call(phase) in (4, 5)
+    assert tp_call(phase, T=0) == 0
+
+
+@pytest.mark.parametrize("phase", [0, 1, 2])
+@pytest.mark.parametrize("change,status", [
+    (dict(Hs=900), 1),                       # not a multiple of 8
+    (dict(Hs=0), 1),
+    (dict(sums_row=9), 1),                   # < 2N
+    (dict(S=9), 1),
+    (dict(T=-1), 1),
+    (dict(sums=0), 1),
+    (dict(sums=addr(7, 2)), 2),              # floats want 4-byte alignment
+    (dict(prefix=addr(0, 8)), 2),
+    (dict(flags=ar.FLAG_SPLIT(7)), 1),       # one launch shape: only PDL
+    (dict(flags=ar.FLAG_KERNEL(2)), 1),
+])
+def test_tp_rejections(lib, phase, change, status):
+    assert tp_call(phase, **change) == status
+
+
+def test_tp_phase_specific_rejections(lib):
+    assert tp_call(1, Hfull=HS - 8) == 1                # full width below the shard's
+    assert tp_call(2, Hfull=HS - 8) == 1
+    assert tp_call(1, sq=0) == 1                         # sq is the output of phase 1
+    assert tp_call(2, sq=0) == 1                         # the output norm needs sq
+    assert tp_call(1, sq=addr(8, 2)) == 2
+    assert tp_call(0, res_w=0) == 1                      # phase 0 reads the weights
+    assert tp_call(2, out=0) == 1                        # phase 2 writes out
+    assert tp_call(2, onw=addr(5, 8)) == 2
+    assert tp_call(0, sums=addr(0, 64)) == 3             # sums written over prefix
+    assert tp_call(1, sq=addr(7, 8)) == 3                # sq written over sums
+    assert tp_call(2, out=addr(7)) == 3                  # out written over sums
+    assert tp_call(2, widx=8) == 1
+    import torch
+    if not torch.cuda.is_available():
+        # reading sums that overlap an input is fine
+        assert tp_call(1, sums=addr(1, 64)) in (4, 5)
+        assert tp_call(2, sq=0, onorm=False) in (4, 5)   # no output norm: sq unused
+        assert tp_call(0, flags=ar.FLAG_PDL) in (4, 5)
+        assert tp_call(0, onorm=False, res_w=addr(3), rms_w=addr(4), out=0) in (4, 5)
+
+
+def test_tp_sums_width(lib):
+    assert lib.attn_res_tp_sums_width(8, 0) == 18
+    assert lib.attn_res_tp_sums_width(8, 1) == 18 + 36
+    assert lib.attn_res_tp_sums_width(0, 1) == 2
+    assert lib.attn_res_tp_sums_width(4, 1) == 10 + 10
+    assert lib.attn_res_tp_sums_width(9, 0) == -1
+    assert lib.attn_res_tp_sums_width(-1, 1) == -1
+    from attention_residual_fusion_gb300 import tp
+    for S in range(9):
+        for g in (0, 1):
+            assert tp.sums_width(S, bool(g)) == lib.attn_res_tp_sums_width(S, g)
+
+
+def test_tp_gram_flag(lib):
+    G = ar.FLAG_TP_GRAM
+    assert tp_call(1, flags=G) == 1                       # no sq phase in the Gram form
+    assert tp_call(0, flags=G) == 1                       # sums_row 10 < 10 + 10
+    assert tp_call(2, flags=G) == 1
+    import torch
+    if not torch.cuda.is_available():
+        assert tp_call(0, flags=G, sums_row=20) in (4, 5)
+        assert tp_call(2, flags=G | ar.FLAG_PDL, sums_row=20, sq=0) in (4, 5)  # sq unused
+        assert tp_call(2, flags=G, sums_row=20, sq=addr(0, 2)) in (4, 5)       # not checked
