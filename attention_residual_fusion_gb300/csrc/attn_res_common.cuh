@@ -11,6 +11,7 @@ namespace attn_res_dev {
 constexpr int kH = 7168;        // hidden size
 constexpr int kVec = 8;         // bf16 per 16-byte vector
 constexpr int kNV = kH / kVec;  // 896 vectors per row
+constexpr float kInvH = 1.0f / kH;  // mean over the row as a product
 
 struct Params {
   uint16_t* prefix;

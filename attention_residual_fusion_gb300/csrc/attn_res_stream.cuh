@@ -5,10 +5,11 @@
 // attn_res_token.cuh), but each cluster loops over many tokens and keeps the
 // HBM stream going while it computes:
 //
-//   * thread 0 of each CTA issues bulk copies (cp.async.bulk, the TMA
-//     engine's one-dimensional form) of the CTA's slice of the token's bank
-//     rows into one stage of a STAGES-deep shared-memory ring; the copies
-//     complete on the stage's `full` mbarrier (expect-tx of the stage bytes);
+//   * the lanes of warp 0 of each CTA issue bulk copies (cp.async.bulk, the
+//     TMA engine's one-dimensional form; one lane per bank row) of the CTA's
+//     slice of the token's bank rows into one stage of a STAGES-deep
+//     shared-memory ring; the copies complete on the stage's `full` mbarrier
+//     (expect-tx of the stage bytes);
 //   * each thread loads its vectors of the token's prefix and delta rows
 //     straight into registers one token ahead, so the ring holds bank rows
 //     only -- shared memory, not registers, is what limits how many CTAs
@@ -18,9 +19,9 @@
 //     vectors straight from the stage, once for the partial sums and once for
 //     the mix;
 //   * after its last read of the stage each warp arrives on the stage's
-//     `empty` mbarrier; thread 0 waits on it, fences the generic-proxy reads
-//     against the async proxy and refills the stage with the token STAGES
-//     ahead;
+//     `empty` mbarrier; thread 0 waits on it, the issuing lanes fence the
+//     generic-proxy reads against the async proxy and refill the stage with
+//     the token STAGES ahead;
 //   * dependents of a PDL launch are released only when this CTA has run
 //     out of tokens (the grid holds every SM until then);
 //   * the token phases run software-pipelined: B(j) (softmax, mix), refill,
@@ -113,14 +114,17 @@ __global__ void __launch_bounds__(StreamCfg<S, HAS_DELTA, HAS_ONORM, K, VPT, STA
     __syncthreads();
   }
 
-  // producer side (thread 0): the bank rows of one token into one stage
+  // producer side (every lane of warp 0): the bank rows of one token into one
+  // stage -- lane 0 arms the stage's barrier with the byte count, then lane i
+  // < S issues the copy of bank row i, so the S copies go out as one warp
+  // instruction
   auto issue_bank = [&](int64_t t, int s) {
     const uint32_t bar = smem_addr(&full_bar[s]);
-    mbar_arrive_expect_tx(bar, C::STAGE_BYTES);
-    const uint16_t* bp = p.blocks + t * p.blocks_token + slice0;
-#pragma unroll
-    for (int i = 0; i < S; ++i)
-      bulk_load(ring_addr + (uint32_t)(s * S + i) * C::SLICE_BYTES, bp + (int64_t)i * p.blocks_slot,
+    if (lane == 0) mbar_arrive_expect_tx(bar, C::STAGE_BYTES);
+    __syncwarp();
+    if (lane < S)
+      bulk_load(ring_addr + (uint32_t)(s * S + lane) * C::SLICE_BYTES,
+                p.blocks + t * p.blocks_token + slice0 + (int64_t)lane * p.blocks_slot,
                 C::SLICE_BYTES, bar);
   };
   // every thread: its vectors of the token's prefix and delta rows
@@ -140,10 +144,10 @@ __global__ void __launch_bounds__(StreamCfg<S, HAS_DELTA, HAS_ONORM, K, VPT, STA
   // tracks the stages whose last issued copies it has not yet seen complete,
   // and that issue's parity.
   uint32_t pending = 0, pending_parity = 0;
-  if (tid == 0) {
+  if (warp == 0) {
     for (int s = 0; s < STAGES && s < ntok; ++s) {
       issue_bank(cid + s * ncl, s);
-      pending |= 1u << s;  // first use of every stage: parity 0
+      pending |= 1u << s;  // first use of every stage: parity 0 (tracked by thread 0)
     }
   }
   // weights: read-only, independent of the preceding kernel
@@ -209,10 +213,18 @@ __global__ void __launch_bounds__(StreamCfg<S, HAS_DELTA, HAS_ONORM, K, VPT, STA
         },
         c_cur, acc);
 
-    // refill stage s with the token STAGES ahead once every local warp is done
-    if (tid == 0 && !failed && j + STAGES < ntok) {
-      wait_or_flag(smem_addr(&empty_bar[s]), sparity, failed, p.err, kErrStageTimeout);
-      if (!failed) {
+    // refill stage s with the token STAGES ahead once every local warp is
+    // done: thread 0 waits and decides for warp 0; each issuing lane orders
+    // the warps' reads of the stage before its copy with a proxy fence
+    if (warp == 0 && j + STAGES < ntok) {
+      bool go = false;
+      if (lane == 0 && !failed) {
+        wait_or_flag(smem_addr(&empty_bar[s]), sparity, failed, p.err, kErrStageTimeout);
+        go = !failed;
+      }
+      go = __shfl_sync(0xffffffffu, go, 0);
+      __syncwarp();
+      if (go) {
         fence_proxy_async_smem();
         issue_bank(cid + (j + STAGES) * ncl, s);
         pending |= 1u << s;

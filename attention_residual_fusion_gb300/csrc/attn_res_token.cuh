@@ -190,11 +190,14 @@ __device__ __forceinline__ void token_mix(Row row,
     }
     const float dtv = __shfl_sync(0xffffffffu, tot, (lane + N) & 31);
     float logit = __int_as_float(0xff800000u);  // -inf
-    if (lane < N) logit = dtv / sqrtf(tot / (float)kH + eps);
+    // reciprocal square root and a fast quotient (z in [1, N]): a few ulp of
+    // fp32 on the weights, far below the bf16 output's resolution, and the
+    // same instructions in every warp, so the weights stay bit-identical
+    if (lane < N) logit = dtv * rsqrtf(fmaf(tot, kInvH, eps));
     const float m = warp_max(logit);
     const float e = (lane < N) ? expf(logit - m) : 0.f;
     const float z = warp_sum(e);
-    const float wl = e / z;
+    const float wl = __fdividef(e, z);
 #pragma unroll
     for (int v = 0; v < VPT; ++v)
 #pragma unroll
@@ -233,7 +236,7 @@ __device__ __forceinline__ void token_finish(typename TokenCfg<S, HAS_DELTA, HAS
   if constexpr (HAS_ONORM) {
     wait_or_flag(smem_addr(&mb.bar_sq[b]), parity, failed, err, kErrExchangeTimeout);
     const float tot = warp_sum(lane < K * NW ? mb.sq[b][lane] : 0.f);
-    const float ro = 1.0f / sqrtf(tot / (float)kH + out_eps);
+    const float ro = rsqrtf(fmaf(tot, kInvH, out_eps));
     const f32x2 ro2 = f2_make(ro, ro);
 #pragma unroll
     for (int v = 0; v < VPT; ++v)
