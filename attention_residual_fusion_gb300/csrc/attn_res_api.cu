@@ -413,10 +413,9 @@ Region floats_region(const void* p, int64_t T, int64_t row, int64_t width, bool 
 
 // Threads per CTA of the sharded kernels: one 16-byte vector per thread where
 // the shard fits in 256 threads, in whole warps.
-int tp_threads(int64_t Hs) {
+int tp_threads(int64_t Hs, int cap) {
   const int64_t nv = Hs / 8;
-  return static_cast<int>(nv >= attn_res_dev::kTpMaxThreads ? attn_res_dev::kTpMaxThreads
-                                                            : ((nv + 31) / 32) * 32);
+  return static_cast<int>(nv >= cap ? cap : ((nv + 31) / 32) * 32);
 }
 
 // One phase of the hidden-sharded mixture: shared checks and launch.
@@ -478,7 +477,8 @@ attn_res_status_t run_tp(int phase, int64_t Hs, int64_t H, attn_res_bf16_t* pref
   ta.sq = uses_sq ? sq : nullptr;
   TpLaunchFn fn = lookup_tp(num_blocks, phase, delta != nullptr, onorm, gram);
   if (fn == nullptr) return ATTN_RES_EINVAL;
-  const int threads = tp_threads(Hs);
+  const int threads = tp_threads(Hs, (phase == 0 && gram) ? attn_res_dev::kTpGramThreads
+                                                          : attn_res_dev::kTpMaxThreads);
   cudaError_t e = status_word(dev, &p.err);
   if (e == cudaSuccess)
     e = fn(p, ta, T, threads, (layout->flags & ATTN_RES_FLAG_PDL) != 0,

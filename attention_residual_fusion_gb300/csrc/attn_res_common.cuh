@@ -235,8 +235,8 @@ __device__ __forceinline__ float warp_max(float v) {
   return v;
 }
 
-constexpr int pow2_at_least(int n) { return n <= 1 ? 1 : 2 * pow2_at_least((n + 1) / 2); }
-constexpr int log2_exact(int n) { return n <= 1 ? 0 : 1 + log2_exact(n / 2); }
+__host__ __device__ constexpr int pow2_at_least(int n) { return n <= 1 ? 1 : 2 * pow2_at_least((n + 1) / 2); }
+__host__ __device__ constexpr int log2_exact(int n) { return n <= 1 ? 0 : 1 + log2_exact(n / 2); }
 
 // Reduce P values (P a power of two, <= 32) across the warp, one sum per
 // value: each butterfly step halves the values a lane carries, exchanging the

@@ -35,6 +35,9 @@ namespace attn_res_dev {
 
 constexpr int kTpMaxThreads = 256;
 constexpr int kTpMaxWarps = kTpMaxThreads / 32;
+// The Gram form of tp_sums keeps ~130 values live per thread: at most 128
+// threads per CTA, so the register budget is not capped below that.
+constexpr int kTpGramThreads = 128;
 
 struct TpArgs {
   int64_t Hs;        // shard width (multiple of 8)
@@ -51,16 +54,39 @@ struct TpCfg {
   static constexpr int NG = N * (N - 1) / 2;  // g_ij, i < j
 };
 
+// Warp totals of values [B, B + P) of v (zero beyond NR) into scratch[warp]:
+// one reduce-scatter butterfly, after which lane l holds the total of value
+// l >> (5 - log2 P).
+template <int NR, int B, int P>
+__device__ __forceinline__ void warp_totals(const float (&v)[NR], float (*scratch)[NR], int warp,
+                                            int lane) {
+  float a[P];
+#pragma unroll
+  for (int r = 0; r < P; ++r) a[r] = (B + r < NR) ? v[B + r < NR ? B + r : 0] : 0.f;
+  const float tot = reduce_scatter<P>(a, lane);
+  constexpr int SH = 5 - log2_exact(P);
+  const int idx = lane >> SH;
+  if ((lane & ((1 << SH) - 1)) == 0 && B + idx < NR) scratch[warp][B + idx] = tot;
+}
+
+// Warp totals of all NR values, in butterflies of at most 16 values (a wider
+// one keeps more values live at once than the registers hold).
+template <int NR, int B>
+__device__ __forceinline__ void warp_groups(const float (&v)[NR], float (*scratch)[NR], int warp,
+                                            int lane) {
+  if constexpr (B < NR) {
+    constexpr int P = (NR - B) >= 16 ? 16 : pow2_at_least(NR - B);
+    warp_totals<NR, B, P>(v, scratch, warp, lane);
+    warp_groups<NR, B + P>(v, scratch, warp, lane);
+  }
+}
+
 // Sum NR per-thread values over the CTA.  The CTA totals end in
 // scratch[0][r], readable by any thread after the call.
 template <int NR>
 __device__ __forceinline__ void cta_sum(const float (&v)[NR], float (*scratch)[NR]) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-#pragma unroll
-  for (int r = 0; r < NR; ++r) {
-    const float s = warp_sum(v[r]);
-    if (lane == 0) scratch[warp][r] = s;
-  }
+  warp_groups<NR, 0>(v, scratch, warp, lane);
   __syncthreads();
   for (int r = threadIdx.x; r < NR; r += blockDim.x) {
     float s = scratch[0][r];
@@ -80,61 +106,85 @@ __device__ __forceinline__ uint4 tp_bank(const Params& p, int64_t t, int i, int6
   return ld_row(p.blocks + t * p.blocks_token + (int64_t)i * p.blocks_slot + col);
 }
 
-// x_i = bank row i (i < S) or the current row c (i == S), widened to fp32.
+// x_i = bank row i (i < S) or the current row c (i == S), widened to fp32
+// pairs.
 template <int S, bool HAS_DELTA>
 __device__ __forceinline__ void tp_sources(const Params& p, int64_t t, int64_t col,
-                                           float (&x)[S + 1][kVec]) {
+                                           f32x2 (&x)[S + 1][4]) {
 #pragma unroll
   for (int i = 0; i <= S; ++i) {
     const uint4 v = (i < S) ? tp_bank(p, t, i < S ? i : 0, col) : tp_current<HAS_DELTA>(p, t, col);
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      x[i][2 * k] = bf_lo(vword(v, k));
-      x[i][2 * k + 1] = bf_hi(vword(v, k));
-    }
+    for (int k = 0; k < 4; ++k) x[i][k] = bf2_widen(vword(v, k));
   }
 }
 
 template <int S, bool HAS_DELTA, bool GRAM>
-__global__ void __launch_bounds__(kTpMaxThreads) attn_res_tp_sums_kernel(const Params p, const TpArgs a) {
+__global__ void __launch_bounds__(GRAM ? kTpGramThreads : kTpMaxThreads)
+    attn_res_tp_sums_kernel(const Params p, const TpArgs a) {
   using C = TpCfg<S>;
   constexpr int N = C::N, NR = C::NR, NT = NR + (GRAM ? C::NG : 0);
   __shared__ float scratch[kTpMaxWarps][NT];
   const int64_t t = blockIdx.x;
   const int64_t nv = a.Hs / kVec;
   grid_dep_wait();
+  // Without Gram entries the 2N sums accumulate as fp32 pairs; with them every
+  // accumulator is a scalar, which keeps the register count (and so the
+  // number of resident CTAs) within reach of the plain form.
   float part[NT];
 #pragma unroll
   for (int r = 0; r < NT; ++r) part[r] = 0.f;
+  f32x2 ss[GRAM ? 1 : N], dt[GRAM ? 1 : N];
+#pragma unroll
+  for (int i = 0; i < (GRAM ? 1 : N); ++i) ss[i] = dt[i] = 0ull;  // +0.0f pairs
   for (int64_t v = threadIdx.x; v < nv; v += blockDim.x) {
     const int64_t col = v * kVec;
     const uint4 rw = ld_weight(p.rms_w + col), qw = ld_weight(p.res_w + col);
-    float q[kVec];
+    f32x2 q[4];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      q[2 * k] = bf_lo(vword(rw, k)) * bf_lo(vword(qw, k));
-      q[2 * k + 1] = bf_hi(vword(rw, k)) * bf_hi(vword(qw, k));
-    }
-    float x[N][kVec];
+    for (int k = 0; k < 4; ++k) q[k] = f2_mul(bf2_widen(vword(rw, k)), bf2_widen(vword(qw, k)));
+    f32x2 x[N][4];
     tp_sources<S, HAS_DELTA>(p, t, col, x);
-#pragma unroll
-    for (int i = 0; i < N; ++i) {
-#pragma unroll
-      for (int k = 0; k < kVec; ++k) {
-        part[i] = fmaf(x[i][k], x[i][k], part[i]);
-        part[N + i] = fmaf(x[i][k], q[k], part[N + i]);
-      }
-    }
-    if constexpr (GRAM) {
-      int g = NR;
+    if constexpr (!GRAM) {
 #pragma unroll
       for (int i = 0; i < N; ++i) {
 #pragma unroll
-        for (int j = i + 1; j < N; ++j, ++g) {
-#pragma unroll
-          for (int k = 0; k < kVec; ++k) part[g] = fmaf(x[i][k], x[j][k], part[g]);
+        for (int k = 0; k < 4; ++k) {
+          ss[i] = f2_fma(x[i][k], x[i][k], ss[i]);
+          dt[i] = f2_fma(x[i][k], q[k], dt[i]);
         }
       }
+    } else {
+#pragma unroll
+      for (int i = 0; i < N; ++i) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float lo = f2_lo(x[i][k]), hi = f2_hi(x[i][k]);
+          part[i] = fmaf(hi, hi, fmaf(lo, lo, part[i]));
+          part[N + i] = fmaf(hi, f2_hi(q[k]), fmaf(lo, f2_lo(q[k]), part[N + i]));
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < N; ++i) {
+#pragma unroll
+        for (int j = 0; j < N; ++j) {
+          if (j > i) {
+            const int g = NR + i * N - i * (i + 1) / 2 + (j - i - 1);  // row-major over i < j
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              part[g] = fmaf(f2_lo(x[i][k]), f2_lo(x[j][k]), part[g]);
+              part[g] = fmaf(f2_hi(x[i][k]), f2_hi(x[j][k]), part[g]);
+            }
+          }
+        }
+      }
+    }
+  }
+  if constexpr (!GRAM) {
+#pragma unroll
+    for (int i = 0; i < N; ++i) {
+      part[i] = f2_lo(ss[i]) + f2_hi(ss[i]);
+      part[N + i] = f2_lo(dt[i]) + f2_hi(dt[i]);
     }
   }
   cta_sum<NT>(part, scratch);
@@ -142,7 +192,10 @@ __global__ void __launch_bounds__(kTpMaxThreads) attn_res_tp_sums_kernel(const P
   grid_dep_launch_dependents();
 }
 
-// Softmax weights of token t from the reduced sums (every thread).
+// Softmax weights of token t from the reduced sums: lane i < N of every warp
+// takes logit i, the warp reduces, and the weights are broadcast to all lanes
+// (every thread of the warp must call).  Same instructions as the unsharded
+// kernels' softmax, so every warp gets bit-identical weights.
 template <int S>
 __device__ __forceinline__ void tp_weights(const TpArgs& a, float eps, int64_t t, float (&w)[S + 1]) {
   constexpr int N = S + 1;
@@ -150,39 +203,31 @@ __device__ __forceinline__ void tp_weights(const TpArgs& a, float eps, int64_t t
     w[0] = 1.f;  // a single source takes all the weight
     return;
   }
+  const int lane = threadIdx.x & 31;
   const float* s = a.sums + t * a.sums_row;
-  float logit[N];
-  float m = __int_as_float(0xff800000u);
+  float logit = __int_as_float(0xff800000u);  // -inf
+  if (lane < N) logit = s[N + lane] * rsqrtf(fmaf(s[lane], a.inv_h, eps));
+  const float m = warp_max(logit);
+  const float e = (lane < N) ? expf(logit - m) : 0.f;
+  const float z = warp_sum(e);
+  const float wl = __fdividef(e, z);
 #pragma unroll
-  for (int i = 0; i < N; ++i) {
-    logit[i] = s[N + i] / sqrtf(s[i] * a.inv_h + eps);
-    m = fmaxf(m, logit[i]);
-  }
-  float z = 0.f;
-#pragma unroll
-  for (int i = 0; i < N; ++i) {
-    w[i] = expf(logit[i] - m);
-    z += w[i];
-  }
-#pragma unroll
-  for (int i = 0; i < N; ++i) w[i] = w[i] / z;
+  for (int i = 0; i < N; ++i) w[i] = __shfl_sync(0xffffffffu, wl, i);
 }
 
 template <int S, bool HAS_DELTA>
 __device__ __forceinline__ void tp_mix(const Params& p, int64_t t, int64_t col, const float (&w)[S + 1],
-                                       uint4& c, float (&acc)[kVec]) {
+                                       uint4& c, f32x2 (&acc)[4]) {
   constexpr int N = S + 1;
   c = tp_current<HAS_DELTA>(p, t, col);
 #pragma unroll
-  for (int k = 0; k < kVec; ++k) acc[k] = 0.f;
+  for (int k = 0; k < 4; ++k) acc[k] = 0ull;
 #pragma unroll
   for (int i = 0; i < N; ++i) {
     const uint4 x = (i < S) ? tp_bank(p, t, i < S ? i : 0, col) : c;
+    const f32x2 w2 = f2_make(w[i], w[i]);
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      acc[2 * k] = fmaf(w[i], bf_lo(vword(x, k)), acc[2 * k]);
-      acc[2 * k + 1] = fmaf(w[i], bf_hi(vword(x, k)), acc[2 * k + 1]);
-    }
+    for (int k = 0; k < 4; ++k) acc[k] = f2_fma(w2, bf2_widen(vword(x, k)), acc[k]);
   }
 }
 
@@ -194,14 +239,15 @@ __global__ void __launch_bounds__(kTpMaxThreads) attn_res_tp_sq_kernel(const Par
   grid_dep_wait();
   float w[S + 1];
   tp_weights<S>(a, p.eps, t, w);
-  float sq[1] = {0.f};
+  f32x2 sq2 = 0ull;
   for (int64_t v = threadIdx.x; v < nv; v += blockDim.x) {
     uint4 c;
-    float acc[kVec];
+    f32x2 acc[4];
     tp_mix<S, HAS_DELTA>(p, t, v * kVec, w, c, acc);
 #pragma unroll
-    for (int k = 0; k < kVec; ++k) sq[0] = fmaf(acc[k], acc[k], sq[0]);
+    for (int k = 0; k < 4; ++k) sq2 = f2_fma(acc[k], acc[k], sq2);
   }
+  const float sq[1] = {f2_lo(sq2) + f2_hi(sq2)};
   cta_sum<1>(sq, scratch);
   if (threadIdx.x == 0) a.sq[t] = scratch[0][0];
   grid_dep_launch_dependents();
@@ -234,25 +280,23 @@ __global__ void __launch_bounds__(kTpMaxThreads) attn_res_tp_finish_kernel(const
   float ro = 1.f;
   if constexpr (HAS_ONORM) {
     const float sq = GRAM ? tp_gram_sq<S>(a, t, w) : a.sq[t];
-    ro = 1.0f / sqrtf(sq * a.inv_h + p.out_eps);
+    ro = rsqrtf(fmaf(sq, a.inv_h, p.out_eps));
   }
   // each thread writes only the vectors it alone reads: no barrier needed
+  const f32x2 ro2 = f2_make(ro, ro);
   for (int64_t v = threadIdx.x; v < nv; v += blockDim.x) {
     const int64_t col = v * kVec;
     uint4 c;
-    float acc[kVec];
+    f32x2 acc[4];
     tp_mix<S, HAS_DELTA>(p, t, col, w, c, acc);
     if constexpr (HAS_ONORM) {
       const uint4 ow = ld_weight(p.onw + col);
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        acc[2 * k] = acc[2 * k] * ro * bf_lo(vword(ow, k));
-        acc[2 * k + 1] = acc[2 * k + 1] * ro * bf_hi(vword(ow, k));
-      }
+      for (int k = 0; k < 4; ++k) acc[k] = f2_mul(f2_mul(acc[k], ro2), bf2_widen(vword(ow, k)));
     }
     st_row(p.out + t * p.out_row + col,
-           make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
-                      pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7])));
+           make_uint4(pack_bf16x2(f2_lo(acc[0]), f2_hi(acc[0])), pack_bf16x2(f2_lo(acc[1]), f2_hi(acc[1])),
+                      pack_bf16x2(f2_lo(acc[2]), f2_hi(acc[2])), pack_bf16x2(f2_lo(acc[3]), f2_hi(acc[3]))));
     if (HAS_DELTA) st_row(p.prefix + t * p.prefix_row + col, c);
     if (p.write_idx >= 0)
       st_row(p.blocks + t * p.blocks_token + (int64_t)p.write_idx * p.blocks_slot + col, c);
