@@ -64,6 +64,7 @@ class Workload:
     out_eps: float = 1e-6
     H: int = HIDDEN
     meta: dict = field(default_factory=dict)
+    group: int = 1  # token rows per bank row (bank has ceil(T / group) rows)
 
     @property
     def slot_stride(self) -> int:
@@ -81,7 +82,7 @@ class Workload:
             None if self.delta is None else self.delta.copy(), self.bank.copy(),
             self.rms_w.copy(), self.res_w.copy(),
             None if self.out_norm_w is None else self.out_norm_w.copy(),
-            self.eps, self.out_eps, self.H, dict(self.meta))
+            self.eps, self.out_eps, self.H, dict(self.meta), self.group)
 
     def algorithmic_bytes(self) -> int:
         """Bytes the mixture must move once: source rows read, delta read,
@@ -90,8 +91,9 @@ class Workload:
         d = 1 if self.has_delta else 0
         w = 1 if self.block_write_idx >= 0 else 0
         o = 1 if self.has_out_norm else 0
-        per_token = R * (self.num_blocks + 1 + d + 1 + d + w)
-        return self.T * per_token + R * (2 + o)
+        bank_rows = -(-self.T // self.group)
+        return (self.T * R * (1 + d + 1 + d) + bank_rows * R * (self.num_blocks + w)
+                + R * (2 + o))
 
 
 def _activations(rng: np.random.Generator, shape: Tuple[int, ...],
@@ -110,7 +112,7 @@ def make_workload(T: int, num_blocks: int, *, capacity: int = 8,
                   slot_scale: Optional[Tuple[float, float]] = None,
                   mixing: bool = False, eps: float = 1e-6,
                   out_eps: float = 1e-6, name: str = "",
-                  token_chunk: int = 256) -> Workload:
+                  token_chunk: int = 256, group: int = 1) -> Workload:
     """Draw one workload.  Every tensor has its own child seed, so changing
     one option does not reshuffle the others."""
     if slot_stride is None:
@@ -136,12 +138,15 @@ def make_workload(T: int, num_blocks: int, *, capacity: int = 8,
     rng_b = np.random.default_rng(s_bank)
     prefix = np.empty((T, H), dtype=np.uint16)
     delta = np.empty((T, H), dtype=np.uint16) if has_delta else None
-    bank = np.full((T, capacity, slot_stride), CANARY, dtype=np.uint16)
+    TB = -(-T // group)  # bank rows
+    bank = np.full((TB, capacity, slot_stride), CANARY, dtype=np.uint16)
     for t0 in range(0, T, token_chunk):
         t1 = min(T, t0 + token_chunk)
         prefix[t0:t1] = f32_to_bf16_bits(_activations(rng_p, (t1 - t0, H), outliers))
         if has_delta:
             delta[t0:t1] = f32_to_bf16_bits(_activations(rng_d, (t1 - t0, H), outliers))
+    for t0 in range(0, TB, token_chunk):
+        t1 = min(TB, t0 + token_chunk)
         if num_blocks > 0:
             x = _activations(rng_b, (t1 - t0, num_blocks, H), outliers)
             x *= scales[None, :num_blocks, None]
@@ -150,7 +155,7 @@ def make_workload(T: int, num_blocks: int, *, capacity: int = 8,
                     has_delta, has_out_norm, block_write_idx, prefix, delta,
                     bank, rms_w, res_w, onw if has_out_norm else None, eps,
                     out_eps, H, dict(seed=seed, outliers=outliers,
-                                     slot_scale=slot_scale, mixing=mixing))
+                                     slot_scale=slot_scale, mixing=mixing), group)
 
 
 # ---- the named workloads -------------------------------------------------

@@ -50,7 +50,7 @@ class Oracle:
         lib.attn_res_ref.argtypes = [
             _U16P, _U16P, _U16P, ctypes.c_int, ctypes.c_int, ctypes.c_int,
             _U16P, _U16P, _U16P, ctypes.c_float, ctypes.c_float, _U16P,
-            i64, i64, i64, i64, i64, i64, i64, _F64P, _F64P, ctypes.c_int]
+            i64, i64, i64, i64, i64, i64, i64, i64, _F64P, _F64P, ctypes.c_int]
         lib.attn_res_ref_round_bf16.restype = None
         lib.attn_res_ref_round_bf16.argtypes = [_F64P, _U16P, i64]
         lib.attn_res_ref_widen_bf16.restype = None
@@ -77,13 +77,14 @@ class Oracle:
                  block_write_idx: int, res_w: np.ndarray, rms_w: np.ndarray,
                  out_norm_w: Optional[np.ndarray], eps: float, out_eps: float,
                  out: Optional[np.ndarray] = None, n_threads: int = 1,
-                 want_weights: bool = False):
+                 want_weights: bool = False, blocks_group: int = 1):
         """Run the oracle in place on numpy uint16 (bf16-bit) arrays.
 
         ``prefix``/``delta``/``out`` are [T, >=H] views with unit inner
         stride; ``blocks`` is a [T, capacity, >=H] view with unit inner stride
-        (padding columns allowed).  ``prefix`` and ``blocks`` are modified in
-        place exactly as the library contract says.  Returns ``out`` (and the
+        (padding columns allowed), or [ceil(T / B), capacity, >=H] with
+        ``blocks_group`` = B > 1 token rows per bank row.  ``prefix`` and
+        ``blocks`` are modified in place exactly as the library contract says.  Returns ``out`` (and the
         softmax weights and logits, [T, S+1] float64, when ``want_weights``).
         """
         T = prefix.shape[0]
@@ -95,7 +96,7 @@ class Oracle:
             assert delta.strides[1] == 2 and delta.shape[0] == T
         cap = bt = bs = 0
         if blocks is not None:
-            assert blocks.strides[2] == 2 and blocks.shape[0] == T
+            assert blocks.strides[2] == 2 and blocks.shape[0] == -(-T // blocks_group)
             cap = blocks.shape[1]
             bt = _elem_stride(blocks, 0)
             bs = _elem_stride(blocks, 1)
@@ -107,7 +108,7 @@ class Oracle:
             block_write_idx, cap, _u16(res_w), _u16(rms_w), _u16(out_norm_w),
             eps, out_eps, _u16(out), T, H, _elem_stride(prefix, 0),
             _elem_stride(delta, 0) if delta is not None else 0, bt, bs,
-            _elem_stride(out, 0), None if w is None else w.ctypes.data_as(_F64P),
+            _elem_stride(out, 0), blocks_group, None if w is None else w.ctypes.data_as(_F64P),
             None if lg is None else lg.ctypes.data_as(_F64P), n_threads)
         if rc != 0:
             raise ValueError(f"oracle rejected the arguments (status {rc})")
@@ -146,13 +147,17 @@ def run_workload(wl, n_threads: int = 1, want_weights: bool = False,
     the run to those token rows.  Returns a dict with ``out``, the updated
     ``prefix`` and ``bank`` (of the selected rows) and optionally weights."""
     o = oracle or default()
+    group = getattr(wl, "group", 1)
+    if group > 1 and tokens is not None:
+        raise ValueError("token sampling needs one bank row per token (group 1)")
     idx = np.arange(wl.T) if tokens is None else np.asarray(tokens)
     prefix = np.ascontiguousarray(wl.prefix[idx])
     delta = None if wl.delta is None else np.ascontiguousarray(wl.delta[idx])
-    bank = np.ascontiguousarray(wl.bank[idx])
+    bank = np.ascontiguousarray(wl.bank if group > 1 else wl.bank[idx])
     res = o.attn_res(prefix, delta, bank[:, :, : wl.H], wl.num_blocks,
                      wl.block_write_idx, wl.res_w, wl.rms_w, wl.out_norm_w,
-                     wl.eps, wl.out_eps, None, n_threads, want_weights)
+                     wl.eps, wl.out_eps, None, n_threads, want_weights,
+                     blocks_group=group)
     d = dict(prefix=prefix, bank=bank, tokens=idx)
     if want_weights:
         d["out"], d["weights"], d["logits"] = res

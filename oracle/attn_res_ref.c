@@ -29,6 +29,8 @@
  *   9. write-backs of c: into prefix when delta is given, into
  *      blocks[t, block_write_idx] when block_write_idx >= 0 -- #54261
  *      summary (Tensor! blocks, block_write_idx, -1 = no write) and excerpt.
+ *  10. the bank row of token t is t / B (B >= 1, default 1) -- the #54261
+ *      excerpt addresses block_res at row tb / B.
  *
  * Every arithmetic step is done in IEEE double; bf16 <-> double conversions
  * are exact in one direction and round-to-nearest-even (written out from the
@@ -41,7 +43,11 @@
  *   - normalised rows and the accumulator are never rounded to bf16;
  *   - the mixed current-layer candidate is the rounded row c;
  *   - all reads of a token see the values from before the call
- *     (read-before-write when block_write_idx < num_blocks).
+ *     (read-before-write when block_write_idx < num_blocks);
+ *   - B (the excerpt's divisor, never defined on the pages) maps B
+ *     consecutive token rows to one bank row; of the rows sharing it, the
+ *     last one's c is what the slot holds after the call, and with B > 1 the
+ *     written slot may not also be a source.
  */
 #include <math.h>
 #include <pthread.h>
@@ -121,6 +127,8 @@ typedef struct {
   uint16_t* out;
   int64_t H;
   int64_t prefix_row, delta_row, blocks_token, blocks_slot, out_row;
+  int64_t group;       /* token rows per bank row (B) */
+  int64_t T;
   double* weights_out; /* [T, N] or NULL */
   double* logits_out;  /* [T, N] or NULL */
   const double* q;     /* [H] pseudo-query, shared read-only */
@@ -134,6 +142,8 @@ static void ref_token(const ref_job* j, int64_t t, uint16_t* c, double* acc,
   const int S = j->num_blocks;
   const int N = S + 1;
   uint16_t* prow = j->prefix + t * j->prefix_row;
+  /* bank row of this token: t / B (the excerpt's block_res row tb / B) */
+  const uint16_t* bank = j->blocks ? j->blocks + (t / j->group) * j->blocks_token : NULL;
 
   /* step 1: current-layer row */
   for (int64_t h = 0; h < H; ++h) {
@@ -149,7 +159,7 @@ static void ref_token(const ref_job* j, int64_t t, uint16_t* c, double* acc,
   /* steps 2-4: per-candidate sum of squares, dot with q, logit */
   for (int i = 0; i < N; ++i) {
     const uint16_t* x =
-        (i < S) ? j->blocks + t * j->blocks_token + (int64_t)i * j->blocks_slot
+        (i < S) ? bank + (int64_t)i * j->blocks_slot
                 : c;
     double s2 = 0.0, sd = 0.0;
     for (int64_t h = 0; h < H; ++h) {
@@ -177,7 +187,7 @@ static void ref_token(const ref_job* j, int64_t t, uint16_t* c, double* acc,
   for (int64_t h = 0; h < H; ++h) acc[h] = 0.0;
   for (int i = 0; i < N; ++i) {
     const uint16_t* x =
-        (i < S) ? j->blocks + t * j->blocks_token + (int64_t)i * j->blocks_slot
+        (i < S) ? bank + (int64_t)i * j->blocks_slot
                 : c;
     for (int64_t h = 0; h < H; ++h) acc[h] += w[i] * bf16_to_double(x[h]);
   }
@@ -194,10 +204,13 @@ static void ref_token(const ref_job* j, int64_t t, uint16_t* c, double* acc,
     for (int64_t h = 0; h < H; ++h) orow[h] = double_to_bf16_rne(acc[h]);
   }
 
-  /* step 9: write-backs, after every read of this token */
+  /* step 9: write-backs, after every read of this token.  With B > 1 token
+   * rows share a bank row; in token order each would overwrite the slot, so
+   * it ends holding the c of the group's last row, which alone writes. */
   if (j->delta) memcpy(prow, c, (size_t)H * sizeof(uint16_t));
-  if (j->block_write_idx >= 0) {
-    uint16_t* dst = j->blocks + t * j->blocks_token +
+  if (j->block_write_idx >= 0 &&
+      (t % j->group == j->group - 1 || t == j->T - 1)) {
+    uint16_t* dst = j->blocks + (t / j->group) * j->blocks_token +
                     (int64_t)j->block_write_idx * j->blocks_slot;
     memcpy(dst, c, (size_t)H * sizeof(uint16_t));
   }
@@ -231,8 +244,11 @@ static void* ref_worker(void* arg) {
  * overwritten with c when delta != NULL; blocks[t, block_write_idx] is
  * overwritten with c when block_write_idx >= 0.  weights_out / logits_out
  * ([T, num_blocks+1], optional) expose the softmax weights and logits.
- * Tokens are split into contiguous ranges over n_threads POSIX threads; the
- * per-token code is the scalar loop above.  Returns 0 on success.
+ * blocks_group (B >= 1) token rows share one bank row: token t reads bank
+ * row t / B, and only the last row of each group writes the slot; with
+ * B > 1 the written slot may not be one of the sources.  Tokens are split
+ * into contiguous ranges over n_threads POSIX threads; the per-token code is
+ * the scalar loop above.  Returns 0 on success.
  */
 int attn_res_ref(uint16_t* prefix, const uint16_t* delta, uint16_t* blocks,
                  int num_blocks, int block_write_idx, int blocks_capacity,
@@ -240,8 +256,12 @@ int attn_res_ref(uint16_t* prefix, const uint16_t* delta, uint16_t* blocks,
                  const uint16_t* out_norm_w, float eps, float out_eps,
                  uint16_t* out, int64_t T, int64_t H, int64_t prefix_row,
                  int64_t delta_row, int64_t blocks_token, int64_t blocks_slot,
-                 int64_t out_row, double* weights_out, double* logits_out,
-                 int n_threads) {
+                 int64_t out_row, int64_t blocks_group, double* weights_out,
+                 double* logits_out, int n_threads) {
+  if (blocks_group < 1) return REF_EINVAL;
+  /* a shared bank row may not be both read and written within one call */
+  if (blocks_group > 1 && block_write_idx >= 0 && block_write_idx < num_blocks)
+    return REF_EINVAL;
   if (T < 0 || H <= 0 || num_blocks < 0 || num_blocks > 8 ||
       num_blocks > blocks_capacity || block_write_idx < -1 ||
       block_write_idx >= blocks_capacity || !prefix || !res_w || !rms_w || !out)
@@ -282,6 +302,8 @@ int attn_res_ref(uint16_t* prefix, const uint16_t* delta, uint16_t* blocks,
     j->blocks_token = blocks_token;
     j->blocks_slot = blocks_slot;
     j->out_row = out_row;
+    j->group = blocks_group;
+    j->T = T;
     j->weights_out = weights_out;
     j->logits_out = logits_out;
     j->q = q;

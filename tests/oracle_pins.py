@@ -301,8 +301,47 @@ def pin_threads_agree(o):
             assert np.array_equal(x, y)
 
 
+def pin_grouped_bank(o):
+    """B token rows per bank row (the excerpt's row index tb / B): the result
+    is the float64 restatement applied to the bank with row t / B repeated
+    for every token row t; the written slot of each bank row ends holding c
+    of the last row of its group; a written slot that is also a source, and
+    B < 1, are rejected."""
+    rng = np.random.default_rng(12)
+    H, S, cap, T = 64, 4, 8, 7
+    for B in (2, 3, 7):
+        for widx in (-1, 6):
+            prefix, delta, _, rms_w, res_w, onw = _case(rng, T, H, S, cap, True, True, widx)
+            TB = -(-T // B)
+            bank = np.full((TB, cap, H), W.CANARY, dtype=np.uint16)
+            bank[:, :S] = _rand_bits(rng, (TB, S, H))
+            p0, b0 = prefix.copy(), bank.copy()
+            out, w, _ = o.attn_res(prefix, delta, bank, S, widx, res_w, rms_w, onw, 1e-6,
+                                   1e-3, want_weights=True, blocks_group=B)
+            expanded = b0[np.arange(T) // B]
+            c, wr, _, y = R.restate(p0, delta, expanded, S, res_w, rms_w, onw, 1e-6, 1e-3)
+            tag = (B, widx)
+            assert np.allclose(w, wr, rtol=1e-10, atol=1e-15), tag
+            assert np.all(R.is_nearest_bf16(out, y, rel_slack=1e-9)), tag
+            assert np.array_equal(prefix, c), tag
+            expect = b0.copy()
+            if widx >= 0:
+                for g in range(TB):
+                    expect[g, widx] = c[min(g * B + B - 1, T - 1)]
+            assert np.array_equal(bank, expect), tag
+    prefix, delta, _, rms_w, res_w, onw = _case(rng, 4, 16, 2, 4, True, True, 1)
+    bank = _rand_bits(rng, (2, 4, 16))
+    for B, widx in ((2, 1), (0, -1)):
+        try:
+            o.attn_res(prefix.copy(), delta, bank.copy() if B else bank[:0], 2, widx, res_w,
+                       rms_w, onw, 1e-6, 1e-6, blocks_group=B)
+        except (ValueError, AssertionError, ZeroDivisionError):
+            continue
+        raise AssertionError(f"blocks_group={B}, write slot {widx} accepted")
+
+
 ALL_PINS = [pin_bf16_rounding, pin_golden_handworked, pin_s0_is_rmsnorm,
             pin_identical_sources, pin_weights_sum_to_one, pin_scale_invariance,
             pin_hard_selection, pin_slot_permutation, pin_two_sources_sigmoid,
             pin_bruteforce_tiny_h, pin_writeback_reads_before_write,
-            pin_threads_agree]
+            pin_threads_agree, pin_grouped_bank]

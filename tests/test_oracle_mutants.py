@@ -51,6 +51,14 @@ MUTANTS = [
      "if (frac >= 0.5) n += 1u;", 1),
     ("rounding_truncates",
      "if (frac > 0.5 || (frac == 0.5 && (n & 1u))) n += 1u;", "", 1),
+    ("grouped_bank_row_modulo",
+     "j->blocks + (t / j->group) * j->blocks_token : NULL;",
+     "j->blocks + (t % j->group) * j->blocks_token : NULL;", 1),
+    ("grouped_first_row_writes",
+     "(t % j->group == j->group - 1 || t == j->T - 1)", "(t % j->group == 0)", 1),
+    ("grouped_write_into_source_accepted",
+     "if (blocks_group > 1 && block_write_idx >= 0 && block_write_idx < num_blocks)",
+     "if (0)", 1),
     ("writeback_before_reads",
      "  /* steps 2-4: per-candidate sum of squares, dot with q, logit */",
      "  if (j->block_write_idx >= 0)\n"
