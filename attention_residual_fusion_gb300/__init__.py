@@ -54,7 +54,7 @@ class Layout(ctypes.Structure):
     _fields_ = [("prefix_row", ctypes.c_int64), ("delta_row", ctypes.c_int64),
                 ("blocks_token", ctypes.c_int64), ("blocks_slot", ctypes.c_int64),
                 ("out_row", ctypes.c_int64), ("blocks_capacity", ctypes.c_int32),
-                ("flags", ctypes.c_uint32)]
+                ("flags", ctypes.c_uint32), ("blocks_group", ctypes.c_int32)]
 
 
 class AttnResError(RuntimeError):
@@ -179,35 +179,41 @@ def check_bf16_cuda(**tensors) -> None:
             raise ValueError(f"{name} must be a CUDA bfloat16 tensor")
 
 
-def make_layout(prefix, delta, blocks, out, flags: int) -> Layout:
+def make_layout(prefix, delta, blocks, out, flags: int, blocks_group: int = 1) -> Layout:
     """attn_res_layout_t from the tensors' strides (row tensors [T, W] and
-    the bank [T, capacity, W], all with unit inner stride; out may be None)."""
+    the bank [ceil(T / blocks_group), capacity, W], all with unit inner
+    stride; out may be None)."""
     for name, t in (("prefix", prefix), ("delta", delta), ("out", out)):
         if t is not None and (t.dim() != 2 or t.stride(1) != 1):
             raise ValueError(f"{name} must be a [T, H] tensor with unit inner stride")
     if blocks is not None and (blocks.dim() != 3 or blocks.stride(2) != 1):
         raise ValueError("blocks must be a [T, capacity, H] tensor with unit inner stride")
+    if blocks is not None and blocks_group >= 1 and \
+            blocks.shape[0] < -(-prefix.shape[0] // blocks_group):
+        raise ValueError("blocks has fewer than ceil(T / blocks_group) token rows")
     return Layout(prefix_row=prefix.stride(0),
                   delta_row=delta.stride(0) if delta is not None else 0,
                   blocks_token=blocks.stride(0) if blocks is not None else 0,
                   blocks_slot=blocks.stride(1) if blocks is not None else 0,
                   out_row=out.stride(0) if out is not None else 0,
                   blocks_capacity=blocks.shape[1] if blocks is not None else 0,
-                  flags=flags)
+                  flags=flags, blocks_group=blocks_group)
 
 
 def attn_res(prefix, delta, blocks, num_blocks: int, block_write_idx: int,
              res_w, rms_w, out_norm_w=None, eps: float = 1e-6,
              out_eps: float = 1e-6, out=None, *, pdl: bool = False,
              split: int = 0, kernel: int = 0, stages: int = 0, vpt: int = 0,
-             stream=None):
+             blocks_group: int = 1, stream=None):
     """AttnRes mixture on CUDA bf16 tensors (see include/attn_res.h); H is
     the length of ``res_w`` (7168 for the tuned kernels, any multiple of 8).
 
     prefix [T, H] (updated in place when ``delta`` is given), delta [T, H] or
     None, blocks [T, capacity, H] (any token/slot strides, unit inner stride;
     slot ``block_write_idx`` is overwritten when >= 0), res_w / rms_w /
-    out_norm_w [H].  Returns ``out`` [T, H] (allocated if not given).
+    out_norm_w [H].  With ``blocks_group`` = B > 1, token row t uses bank row
+    t // B (blocks is [ceil(T / B), capacity, H]).  Returns ``out`` [T, H]
+    (allocated if not given).
     """
     import torch
 
@@ -219,7 +225,7 @@ def attn_res(prefix, delta, blocks, num_blocks: int, block_write_idx: int,
         out = torch.empty((T, H), dtype=prefix.dtype, device=prefix.device)
     lay = make_layout(prefix, delta, blocks, out,
                       (FLAG_PDL if pdl else 0) | FLAG_SPLIT(split) | FLAG_KERNEL(kernel) |
-                      FLAG_STAGES(stages) | FLAG_VPT(vpt))
+                      FLAG_STAGES(stages) | FLAG_VPT(vpt), blocks_group)
     if stream is None:
         stream = torch.cuda.current_stream(prefix.device)
     st = call_raw(_ptr(prefix), _ptr(delta), _ptr(blocks), num_blocks,

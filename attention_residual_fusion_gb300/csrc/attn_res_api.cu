@@ -244,6 +244,11 @@ struct RowArgs {
   Region extra[2] = {};      // float buffers of the hidden-sharded calls
 };
 
+// Token rows per bank row (B); 0 in the layout means 1.
+int64_t bank_group(const attn_res_layout_t* L) {
+  return L->blocks_group > 1 ? L->blocks_group : 1;
+}
+
 // Pointers, strides, alignment and overlaps (pure host checks), then the
 // kernel parameters.  Scalars (num_blocks, write_idx, eps, flags, T >= 0) are
 // checked by the caller first; T must be > 0 here.
@@ -251,6 +256,8 @@ attn_res_status_t check_rows(const RowArgs& a, Params* p) {
   const int64_t H = a.H, T = a.T;
   const attn_res_layout_t* L = a.layout;
   const int cap = L->blocks_capacity;
+  const int64_t group = bank_group(L);
+  const int64_t TB = (T + group - 1) / group;  // bank rows the call touches
   const bool has_delta = a.delta != nullptr;
   const bool has_onorm = a.onw != nullptr;
   const bool uses_bank = a.num_blocks > 0 || (a.writes && a.write_idx >= 0);
@@ -265,7 +272,7 @@ attn_res_status_t check_rows(const RowArgs& a, Params* p) {
     return ATTN_RES_EINVAL;
   if (uses_bank) {
     if (bad_row_stride(bs)) return ATTN_RES_EINVAL;
-    if (T > 1 && (bt < (int64_t)(cap - 1) * bs + H || bt > kMaxStride)) return ATTN_RES_EINVAL;
+    if (TB > 1 && (bt < (int64_t)(cap - 1) * bs + H || bt > kMaxStride)) return ATTN_RES_EINVAL;
   }
   if (!aligned16(a.prefix) || (a.need_weights && (!aligned16(a.res_w) || !aligned16(a.rms_w))) ||
       (a.writes && !aligned16(a.out)) || (has_delta && !aligned16(a.delta)) ||
@@ -276,7 +283,7 @@ attn_res_status_t check_rows(const RowArgs& a, Params* p) {
     return ATTN_RES_EALIGN;
 
   {
-    const int64_t bank_elems = (T - 1) * (T > 1 ? bt : 0) + (int64_t)(cap > 0 ? cap - 1 : 0) * bs + H;
+    const int64_t bank_elems = (TB - 1) * (TB > 1 ? bt : 0) + (int64_t)(cap > 0 ? cap - 1 : 0) * bs + H;
     Region regs[9] = {
         rows_region(a.prefix, T, pr, H, true, a.writes && has_delta),
         rows_region(a.delta, T, dr, H, has_delta, false),
@@ -308,6 +315,8 @@ attn_res_status_t check_rows(const RowArgs& a, Params* p) {
   p->blocks_slot = uses_bank ? bs : 0;
   p->out_row = a.writes ? orow : 0;
   p->write_idx = a.writes ? a.write_idx : -1;
+  p->bank_group = group;
+  p->tokens = T;
   p->err = nullptr;
   return ATTN_RES_OK;
 }
@@ -322,6 +331,9 @@ attn_res_status_t check_scalars(int64_t T, int64_t H, int num_blocks, int write_
   if (num_blocks < 0 || num_blocks > ATTN_RES_MAX_BLOCKS || cap < 0 || num_blocks > cap)
     return ATTN_RES_EINVAL;
   if (write_idx < -1 || write_idx >= cap) return ATTN_RES_EINVAL;
+  if (layout->blocks_group < 0) return ATTN_RES_EINVAL;
+  // rows sharing a bank row may not both read and write one of its slots
+  if (bank_group(layout) > 1 && write_idx >= 0 && write_idx < num_blocks) return ATTN_RES_EINVAL;
   if (!std::isfinite(eps) || eps < 0.f || !std::isfinite(out_eps) || out_eps < 0.f)
     return ATTN_RES_EINVAL;
   if ((layout->flags & ~known) != 0) return ATTN_RES_EINVAL;

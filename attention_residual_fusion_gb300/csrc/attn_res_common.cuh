@@ -22,10 +22,28 @@ struct Params {
   const uint16_t* onw;
   uint16_t* out;
   int64_t prefix_row, delta_row, blocks_token, blocks_slot, out_row;
+  int64_t bank_group;  // B: token rows per bank row (>= 1)
+  int64_t tokens;      // T
   int write_idx;
   float eps, out_eps;
   unsigned* err;  // device status word (error bits)
 };
+
+// Bank row of token row t: t / B, the row index the attn_res_kernel.cu
+// excerpt of vllm PR #54261 gives block_res (tb / B).  T < 2^31.
+__device__ __forceinline__ const uint16_t* bank_of(const Params& p, int64_t t) {
+  const int64_t r = p.bank_group == 1 ? t : (int64_t)((uint32_t)t / (uint32_t)p.bank_group);
+  return p.blocks + r * p.blocks_token;
+}
+// Whether token row t writes its c into the bank slot.  With B > 1 the rows
+// of a group share the slot and the group's last row writes it (the value
+// the slot would hold had the rows written in order); the slot is then never
+// a source, so no row of the group reads it.
+__device__ __forceinline__ bool writes_slot(const Params& p, int64_t t) {
+  if (p.write_idx < 0) return false;
+  if (p.bank_group == 1) return true;
+  return ((uint32_t)t % (uint32_t)p.bank_group) == (uint32_t)(p.bank_group - 1) || t == p.tokens - 1;
+}
 
 // Error bits recorded in the device status word.
 constexpr unsigned kErrStageTimeout = 1u;     // a shared-memory stage never filled

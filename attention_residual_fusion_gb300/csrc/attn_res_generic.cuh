@@ -38,13 +38,15 @@ __global__ void __launch_bounds__(kGenericThreads)
   const int64_t nv = H / kVec;
 
   grid_dep_wait();  // no loads before the producer of prefix / delta is done
+  uint16_t* const bank_row = const_cast<uint16_t*>(bank_of(p, t));
+  const bool slot_write = writes_slot(p, t);
 
   auto current = [&](int64_t col) -> uint4 {
     const uint4 pv = ld_row(p.prefix + t * p.prefix_row + col);
     return HAS_DELTA ? add_bf16x8(pv, ld_row(p.delta + t * p.delta_row + col)) : pv;
   };
   auto bank = [&](int i, int64_t col) -> uint4 {
-    return ld_row(p.blocks + t * p.blocks_token + (int64_t)i * p.blocks_slot + col);
+    return ld_row(bank_row + (int64_t)i * p.blocks_slot + col);
   };
 
   // pass 1: partial sums
@@ -159,8 +161,7 @@ __global__ void __launch_bounds__(kGenericThreads)
            make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
                       pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7])));
     if (HAS_DELTA) st_row(p.prefix + t * p.prefix_row + col, c);
-    if (p.write_idx >= 0)
-      st_row(p.blocks + t * p.blocks_token + (int64_t)p.write_idx * p.blocks_slot + col, c);
+    if (slot_write) st_row(bank_row + (int64_t)p.write_idx * p.blocks_slot + col, c);
   }
   grid_dep_launch_dependents();
 }

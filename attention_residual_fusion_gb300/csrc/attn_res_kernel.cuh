@@ -76,7 +76,7 @@ __global__ void __launch_bounds__(SplitCfg<S, HAS_DELTA, HAS_ONORM, K>::THREADS)
   for (int i = 0; i < ROWS; ++i) x[i] = make_uint4(0, 0, 0, 0);
   uint4 rw = make_uint4(0, 0, 0, 0), qw = rw, ow = rw;
   if (active) {
-    const uint16_t* bp = p.blocks + t * p.blocks_token + col;
+    const uint16_t* bp = bank_of(p, t) + col;
 #pragma unroll
     for (int i = 0; i < S; ++i) x[i] = ld_row(bp + (int64_t)i * p.blocks_slot);
     // 2. weights
@@ -111,8 +111,9 @@ __global__ void __launch_bounds__(SplitCfg<S, HAS_DELTA, HAS_ONORM, K>::THREADS)
   if (active) {
     st_row(p.out + t * p.out_row + col, o[0]);
     if (HAS_DELTA) st_row(p.prefix + t * p.prefix_row + col, c[0]);
-    if (p.write_idx >= 0)
-      st_row(p.blocks + t * p.blocks_token + (int64_t)p.write_idx * p.blocks_slot + col, c[0]);
+    if (writes_slot(p, t))
+      st_row(const_cast<uint16_t*>(bank_of(p, t)) + (int64_t)p.write_idx * p.blocks_slot + col,
+             c[0]);
   }
 }
 

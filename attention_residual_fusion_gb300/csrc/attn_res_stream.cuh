@@ -124,7 +124,7 @@ __global__ void __launch_bounds__(StreamCfg<S, HAS_DELTA, HAS_ONORM, K, VPT, STA
     __syncwarp();
     if (lane < S)
       bulk_load(ring_addr + (uint32_t)(s * S + lane) * C::SLICE_BYTES,
-                p.blocks + t * p.blocks_token + slice0 + (int64_t)lane * p.blocks_slot,
+                bank_of(p, t) + slice0 + (int64_t)lane * p.blocks_slot,
                 C::SLICE_BYTES, bar);
   };
   // every thread: its vectors of the token's prefix and delta rows
@@ -238,6 +238,8 @@ __global__ void __launch_bounds__(StreamCfg<S, HAS_DELTA, HAS_ONORM, K, VPT, STA
     if (j + 1 < ntok) phase_a(j + 1, c_next);
 
     // C(j): output norm and stores
+    const bool slot_write = writes_slot(p, t);
+    uint16_t* const slot = const_cast<uint16_t*>(bank_of(p, t)) + (int64_t)p.write_idx * p.blocks_slot;
     uint4 o[VPT];
     token_finish<S, HAS_DELTA, HAS_ONORM, K, NW, VPT>(mb, b, bparity, lane, p.out_eps, failed,
                                                        p.err, ow, acc, o);
@@ -246,9 +248,7 @@ __global__ void __launch_bounds__(StreamCfg<S, HAS_DELTA, HAS_ONORM, K, VPT, STA
       if (active[v]) {
         st_row(p.out + t * p.out_row + col[v], o[v]);
         if (HAS_DELTA) st_row(p.prefix + t * p.prefix_row + col[v], c_cur[v]);
-        if (p.write_idx >= 0)
-          st_row(p.blocks + t * p.blocks_token + (int64_t)p.write_idx * p.blocks_slot + col[v],
-                 c_cur[v]);
+        if (slot_write) st_row(slot + col[v], c_cur[v]);
       }
       c_cur[v] = c_next[v];
     }

@@ -103,7 +103,7 @@ __device__ __forceinline__ uint4 tp_current(const Params& p, int64_t t, int64_t 
 }
 
 __device__ __forceinline__ uint4 tp_bank(const Params& p, int64_t t, int i, int64_t col) {
-  return ld_row(p.blocks + t * p.blocks_token + (int64_t)i * p.blocks_slot + col);
+  return ld_row(bank_of(p, t) + (int64_t)i * p.blocks_slot + col);
 }
 
 // x_i = bank row i (i < S) or the current row c (i == S), widened to fp32
@@ -284,6 +284,7 @@ __global__ void __launch_bounds__(kTpMaxThreads) attn_res_tp_finish_kernel(const
   }
   // each thread writes only the vectors it alone reads: no barrier needed
   const f32x2 ro2 = f2_make(ro, ro);
+  const bool slot_write = writes_slot(p, t);
   for (int64_t v = threadIdx.x; v < nv; v += blockDim.x) {
     const int64_t col = v * kVec;
     uint4 c;
@@ -298,8 +299,8 @@ __global__ void __launch_bounds__(kTpMaxThreads) attn_res_tp_finish_kernel(const
            make_uint4(pack_bf16x2(f2_lo(acc[0]), f2_hi(acc[0])), pack_bf16x2(f2_lo(acc[1]), f2_hi(acc[1])),
                       pack_bf16x2(f2_lo(acc[2]), f2_hi(acc[2])), pack_bf16x2(f2_lo(acc[3]), f2_hi(acc[3]))));
     if (HAS_DELTA) st_row(p.prefix + t * p.prefix_row + col, c);
-    if (p.write_idx >= 0)
-      st_row(p.blocks + t * p.blocks_token + (int64_t)p.write_idx * p.blocks_slot + col, c);
+    if (slot_write)
+      st_row(const_cast<uint16_t*>(bank_of(p, t)) + (int64_t)p.write_idx * p.blocks_slot + col, c);
   }
   grid_dep_launch_dependents();
 }

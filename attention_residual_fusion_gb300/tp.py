@@ -65,12 +65,12 @@ def _raise(st: int) -> None:
 
 
 def tp_sums(prefix, delta, blocks, num_blocks: int, res_w, rms_w, sums, *,
-            gram: bool = False, pdl: bool = False, stream=None) -> None:
+            gram: bool = False, pdl: bool = False, blocks_group: int = 1, stream=None) -> None:
     """attn_res_tp_sums on the shard: sums[t, :2N] = (sum x_i^2, <x_i, q>),
     then the Gram entries with ``gram``."""
     check_bf16_cuda(prefix=prefix, delta=delta, blocks=blocks, res_w=res_w, rms_w=rms_w)
     _check_f32_cuda(sums=sums)
-    lay = make_layout(prefix, delta, blocks, None, _flags(pdl, gram))
+    lay = make_layout(prefix, delta, blocks, None, _flags(pdl, gram), blocks_group)
     _raise(lib().attn_res_tp_sums(
         res_w.shape[0], _ptr(prefix) or None, _ptr(delta) or None, _ptr(blocks) or None,
         num_blocks, _ptr(res_w) or None, _ptr(rms_w) or None, _ptr(sums) or None,
@@ -78,11 +78,11 @@ def tp_sums(prefix, delta, blocks, num_blocks: int, res_w, rms_w, sums, *,
 
 
 def tp_sq(prefix, delta, blocks, num_blocks: int, H: int, eps: float, sums, sq, *,
-          pdl: bool = False, stream=None) -> None:
+          pdl: bool = False, blocks_group: int = 1, stream=None) -> None:
     """attn_res_tp_sq on the shard: sq[t] = sum over the shard of acc^2."""
     check_bf16_cuda(prefix=prefix, delta=delta, blocks=blocks)
     _check_f32_cuda(sums=sums, sq=sq)
-    lay = make_layout(prefix, delta, blocks, None, FLAG_PDL if pdl else 0)
+    lay = make_layout(prefix, delta, blocks, None, FLAG_PDL if pdl else 0, blocks_group)
     _raise(lib().attn_res_tp_sq(
         prefix.shape[1], H, _ptr(prefix) or None, _ptr(delta) or None, _ptr(blocks) or None,
         num_blocks, eps, _ptr(sums) or None, sums.stride(0), _ptr(sq) or None,
@@ -91,11 +91,12 @@ def tp_sq(prefix, delta, blocks, num_blocks: int, H: int, eps: float, sums, sq, 
 
 def tp_finish(prefix, delta, blocks, num_blocks: int, block_write_idx: int, H: int,
               out_norm_w, eps: float, out_eps: float, sums, sq, out, *,
-              gram: bool = False, pdl: bool = False, stream=None) -> None:
+              gram: bool = False, pdl: bool = False, blocks_group: int = 1,
+              stream=None) -> None:
     """attn_res_tp_finish on the shard: out and the write-backs of c."""
     check_bf16_cuda(prefix=prefix, delta=delta, blocks=blocks, out_norm_w=out_norm_w, out=out)
     _check_f32_cuda(sums=sums, sq=sq)
-    lay = make_layout(prefix, delta, blocks, out, _flags(pdl, gram))
+    lay = make_layout(prefix, delta, blocks, out, _flags(pdl, gram), blocks_group)
     _raise(lib().attn_res_tp_finish(
         prefix.shape[1], H, _ptr(prefix) or None, _ptr(delta) or None, _ptr(blocks) or None,
         num_blocks, block_write_idx, _ptr(out_norm_w) or None, eps, out_eps,
@@ -109,14 +110,14 @@ CUDA_PHASES = types.SimpleNamespace(sums=tp_sums, sq=tp_sq, finish=tp_finish)
 def attn_res_tp(prefix, delta, blocks, num_blocks: int, block_write_idx: int, res_w, rms_w,
                 out_norm_w=None, eps: float = 1e-6, out_eps: float = 1e-6, out=None, *,
                 H: int | None = None, group=None, all_reduce=None, phases=None,
-                gram: bool = False, pdl: bool = False, stream=None):
+                gram: bool = False, pdl: bool = False, blocks_group: int = 1, stream=None):
     """The mixture on this rank's column shard (every row-sized argument is
     the shard, width ``res_w.shape[0]``).  ``H`` is the full width (default:
     shard width x world size of ``group``).  ``all_reduce(tensor)`` sums a
     float32 tensor in place over the ranks (default torch.distributed's
     all_reduce on ``group``; with no process group initialised the call is
-    local).  ``gram`` selects the single-exchange form.  Returns ``out``
-    (allocated if not given)."""
+    local).  ``gram`` selects the single-exchange form; ``blocks_group`` as
+    for attn_res.  Returns ``out`` (allocated if not given)."""
     import torch
     import torch.distributed as dist
 
@@ -138,14 +139,16 @@ def attn_res_tp(prefix, delta, blocks, num_blocks: int, block_write_idx: int, re
         out = torch.empty((T, Hs), dtype=prefix.dtype, device=dev)
     gram = bool(gram and out_norm_w is not None)  # the Gram entries serve the output norm only
     sums = torch.empty((T, sums_width(num_blocks, gram)), dtype=torch.float32, device=dev)
-    ph.sums(prefix, delta, blocks, num_blocks, res_w, rms_w, sums, gram=gram, pdl=pdl,
-            stream=stream)
+    kw = dict(pdl=pdl, stream=stream)
+    if blocks_group != 1:
+        kw["blocks_group"] = blocks_group
+    ph.sums(prefix, delta, blocks, num_blocks, res_w, rms_w, sums, gram=gram, **kw)
     all_reduce(sums)
     sq = None
     if out_norm_w is not None and not gram:
         sq = torch.empty((T,), dtype=torch.float32, device=dev)
-        ph.sq(prefix, delta, blocks, num_blocks, H, eps, sums, sq, pdl=pdl, stream=stream)
+        ph.sq(prefix, delta, blocks, num_blocks, H, eps, sums, sq, **kw)
         all_reduce(sq)
     ph.finish(prefix, delta, blocks, num_blocks, block_write_idx, H, out_norm_w, eps, out_eps,
-              sums, sq, out, gram=gram, pdl=pdl, stream=stream)
+              sums, sq, out, gram=gram, **kw)
     return out

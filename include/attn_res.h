@@ -98,12 +98,26 @@ typedef enum {
 typedef struct {
   int64_t prefix_row;      /* between token rows of prefix (>= H) */
   int64_t delta_row;       /* between token rows of delta (>= H; ignored if delta == NULL) */
-  int64_t blocks_token;    /* between tokens of the bank (>= (capacity-1)*blocks_slot + H when T > 1) */
+  int64_t blocks_token;    /* between token rows of the bank (>= (capacity-1)*blocks_slot + H
+                              when the call touches more than one bank row) */
   int64_t blocks_slot;     /* between slots of one token (>= H) */
   int64_t out_row;         /* between token rows of out (>= H) */
   int32_t blocks_capacity; /* slots allocated per token (blocks.shape[1]); >= num_blocks */
   uint32_t flags;          /* ATTN_RES_FLAG_* */
+  int32_t blocks_group;    /* B: token rows per bank row (0 or 1: one bank row per
+                              token); see "Shared bank rows" below */
 } attn_res_layout_t;
+
+/* Shared bank rows (B = layout.blocks_group > 1).  The attn_res_kernel.cu
+ * excerpt of vllm PR #54261 addresses the bank at row tb / B for token row
+ * tb; the pages never say what B stands for.  Here: token row t reads bank
+ * row t / B (integer division), so the bank holds ceil(T / B) token rows of
+ * blocks_token elements.  Several rows then share one write-back slot; it
+ * ends holding c of the last row of each group (the value sequential writes
+ * in token order would leave), and only that row writes it.  Because the
+ * other rows of the group would read a slot that is being written,
+ * 0 <= block_write_idx < num_blocks is ATTN_RES_EINVAL when B > 1; a
+ * negative blocks_group is ATTN_RES_EINVAL too. */
 
 /*
  * attn_res -- enqueue the AttnRes mixture for T token rows on `stream`.

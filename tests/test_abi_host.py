@@ -157,6 +157,7 @@ def test_append_slot_equal_to_capacity_is_rejected(lib):
     ("prefix_row", H + 4, 2), ("blocks_slot", 7232 + 4, 2), ("out_row", H + 1, 2),
     ("blocks_capacity", -1, 1), ("flags", 0x4, 1), ("flags", ar.FLAG_TP_GRAM, 1), ("flags", ar.FLAG_SPLIT(5), 1),
     ("flags", ar.FLAG_KERNEL(7), 1), ("flags", ar.FLAG_KERNEL(2) | ar.FLAG_SPLIT(16), 1),
+    ("blocks_group", -1, 1),
 ])
 def test_layout_rejections(lib, field, value, status):
     kw = good()
@@ -310,3 +311,38 @@ def test_tp_gram_flag(lib):
         assert tp_call(0, flags=G, sums_row=20) in (4, 5)
         assert tp_call(2, flags=G | ar.FLAG_PDL, sums_row=20, sq=0) in (4, 5)  # sq unused
         assert tp_call(2, flags=G, sums_row=20, sq=addr(0, 2)) in (4, 5)       # not checked
+
+
+def test_shared_bank_rows_host_checks(lib):
+    import ctypes
+    assert ctypes.sizeof(ar.Layout) == 56
+    import torch
+    no_gpu = not torch.cuda.is_available()
+    # a written slot that is also a source is rejected once rows share a bank row
+    kw = good(S=4, widx=2)
+    kw["layout"].blocks_group = 2
+    assert call(**kw) == 1
+    kw["layout"].blocks_group = 1
+    if no_gpu:
+        assert call(**kw) in (4, 5)
+    # a slot that is not a source is fine
+    kw = good(S=4, widx=6)
+    kw["layout"].blocks_group = 2
+    if no_gpu:
+        assert call(**kw) in (4, 5)
+    # T = 4 rows in groups of 4: one bank row, so its token stride is unused
+    kw = good(T=4, S=4, widx=6)
+    kw["layout"].blocks_group = 4
+    kw["layout"].blocks_token = 0
+    if no_gpu:
+        assert call(**kw) in (4, 5)
+    kw["layout"].blocks_group = 2                        # two bank rows: stride checked
+    assert call(**kw) == 1
+    # the bank extent shrinks with B: an out placed after ceil(T/B) bank rows
+    kw = good(T=4, S=4, widx=6)
+    kw["layout"].blocks_group = 4
+    kw["out"] = addr(2, 8 * H * 2 + 4096)                # past one bank row of 8 slots
+    if no_gpu:
+        assert call(**kw) in (4, 5)
+    kw["layout"].blocks_group = 1                        # four bank rows: overlaps
+    assert call(**kw) == 3

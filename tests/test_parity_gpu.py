@@ -301,3 +301,27 @@ def test_generic_kernel_forced_at_full_width(S):
     wl = W.make_workload(33, S, capacity=9, has_delta=True, has_out_norm=True,
                          block_write_idx=8, seed=40 + S, mixing=True)
     full_check(wl, tag=f"generic_forced_S{S}", kernel=ar.KERNEL_GENERIC)
+
+
+# B token rows per bank row (bank row t // B): every kernel, ragged last
+# group, write-back into a slot that is not a source (the group's last row
+# writes it), and the rejection of a written source slot.
+GROUPED = [(B, T, S, w, k) for B in (2, 3, 8) for (T, S, w) in ((5, 4, -1), (37, 8, 8), (300, 8, 8),
+                                                                 (300, 0, 2), (37, 1, 5))
+           for k in (ar.KERNEL_SPLIT, ar.KERNEL_STREAM, ar.KERNEL_GENERIC)]
+
+
+@pytest.mark.parametrize("B,T,S,w,kernel", GROUPED,
+                         ids=[f"B{B}_T{T}_S{S}_w{w}_k{k}" for B, T, S, w, k in GROUPED])
+def test_shared_bank_rows(B, T, S, w, kernel):
+    wl = W.make_workload(T, S, capacity=9, has_delta=bool(T % 2), has_out_norm=True,
+                         block_write_idx=w, seed=70 + B + S, mixing=True, group=B)
+    full_check(wl, tag=f"group{B}_T{T}_S{S}", kernel=kernel)
+
+
+def test_shared_bank_rows_reject_written_source():
+    wl = W.make_workload(6, 4, capacity=8, has_delta=True, has_out_norm=True,
+                         block_write_idx=2, seed=1, group=2)
+    with pytest.raises(ar.AttnResError) as e:
+        G.run_gpu(wl)
+    assert e.value.status == 1

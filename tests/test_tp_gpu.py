@@ -86,7 +86,7 @@ def run_tp_ranks(wl: W.Workload, widths, *, pdl=False, out_row=None, gram=False)
                     g_res.view[a:b], g_rms.view[a:b],
                     None if g_onw is None else g_onw.view[a:b], wl.eps, wl.out_eps,
                     g_out.view[:, a:b], H=H, all_reduce=group.all_reduce_for(r), gram=gram,
-                    pdl=pdl, stream=stream)
+                    pdl=pdl, blocks_group=wl.group, stream=stream)
         except BaseException as e:  # noqa: BLE001 - reported below
             errors.append(e)
             group.barrier.abort()
@@ -210,3 +210,11 @@ def test_zero_tokens_gram():
     w = torch.ones(896, dtype=torch.bfloat16, device="cuda")
     out = tp.attn_res_tp(z, z, bank, 8, 2, w, w, w, H=7168, all_reduce=lambda t: None, gram=True)
     assert out.shape == (0, 896)
+
+
+@pytest.mark.parametrize("B,widx,gram", [(2, -1, False), (3, 8, True), (5, 8, False)])
+def test_shared_bank_rows(B, widx, gram):
+    """B token rows per bank row, over four shards."""
+    wl = W.make_workload(23, 8, capacity=9, has_delta=True, has_out_norm=True,
+                         block_write_idx=widx, seed=60 + B, mixing=True, group=B)
+    tp_check(wl, [W.HIDDEN // 4] * 4, f"tp_group{B}", gram=gram)
