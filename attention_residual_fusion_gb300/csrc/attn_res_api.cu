@@ -45,7 +45,9 @@ struct Plan {
 //    TMA ring, with 4 vectors per thread (one warp per CTA, fewer warps and so
 //    less reduction and exchange work per token) when there are 6 or more bank
 //    rows or an output norm, else 2 vectors per thread (more warps per SM).
-attn_res_status_t make_plan(int64_t T, int num_blocks, bool has_onorm, uint32_t flags, Plan* out) {
+//  * with shared bank rows (B > 1) the stream kernel has one shape, (7,2,2).
+attn_res_status_t make_plan(int64_t T, int num_blocks, bool has_onorm, uint32_t flags, bool grouped,
+                            Plan* out) {
   Plan pl;
   pl.kernel = static_cast<int>((flags >> 16) & 0xfu);
   pl.split = static_cast<int>((flags >> 8) & 0xffu);
@@ -66,8 +68,8 @@ attn_res_status_t make_plan(int64_t T, int num_blocks, bool has_onorm, uint32_t 
   } else if (pl.kernel == ATTN_RES_KERNEL_STREAM) {
     if (pl.split == 0) pl.split = 7;
     if (pl.stages == 0) pl.stages = 2;
-    if (pl.vpt == 0) pl.vpt = (pl.split == 7 && (num_blocks >= 6 || has_onorm)) ? 4 : 2;
-    pl.shape = stream_shape_index(pl.split, pl.vpt, pl.stages);
+    if (pl.vpt == 0) pl.vpt = (!grouped && pl.split == 7 && (num_blocks >= 6 || has_onorm)) ? 4 : 2;
+    pl.shape = stream_shape_index(pl.split, pl.vpt, pl.stages, grouped);
     if (pl.shape < 0) return ATTN_RES_EINVAL;
   } else {
     return ATTN_RES_EINVAL;
@@ -351,7 +353,8 @@ attn_res_status_t run(int64_t H, attn_res_bf16_t* prefix, const attn_res_bf16_t*
       check_scalars(T, H, num_blocks, block_write_idx, eps, out_eps, layout);
   if (st != ATTN_RES_OK) return st;
   Plan plan;
-  if (make_plan(T, num_blocks, out_norm_w != nullptr, layout->flags, &plan) != ATTN_RES_OK)
+  if (make_plan(T, num_blocks, out_norm_w != nullptr, layout->flags, bank_group(layout) > 1,
+                &plan) != ATTN_RES_OK)
     return ATTN_RES_EINVAL;
   // widths other than the one the fast kernels are built for take the
   // general kernel
@@ -568,7 +571,7 @@ attn_res_status_t attn_res_launch_shape(int64_t T, int num_blocks,
   if (T < 0 || num_blocks < 0 || num_blocks > ATTN_RES_MAX_BLOCKS) return ATTN_RES_EINVAL;
   if ((flags & ~kKnownFlags) != 0) return ATTN_RES_EINVAL;
   Plan pl;
-  attn_res_status_t st = make_plan(T, num_blocks, has_out_norm != 0, flags, &pl);
+  attn_res_status_t st = make_plan(T, num_blocks, has_out_norm != 0, flags, false, &pl);
   if (st != ATTN_RES_OK) return st;
   const bool comm = num_blocks > 0 || has_out_norm;
   const bool generic = pl.kernel == ATTN_RES_KERNEL_GENERIC;

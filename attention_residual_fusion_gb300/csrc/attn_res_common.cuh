@@ -31,7 +31,10 @@ struct Params {
 
 // Bank row of token row t: t / B, the row index the attn_res_kernel.cu
 // excerpt of vllm PR #54261 gives block_res (tb / B).  T < 2^31.
+// GROUPED = false: the caller guarantees B == 1 (no test in a token loop).
+template <bool GROUPED = true>
 __device__ __forceinline__ const uint16_t* bank_of(const Params& p, int64_t t) {
+  if constexpr (!GROUPED) return p.blocks + t * p.blocks_token;
   const int64_t r = p.bank_group == 1 ? t : (int64_t)((uint32_t)t / (uint32_t)p.bank_group);
   return p.blocks + r * p.blocks_token;
 }
@@ -39,9 +42,10 @@ __device__ __forceinline__ const uint16_t* bank_of(const Params& p, int64_t t) {
 // of a group share the slot and the group's last row writes it (the value
 // the slot would hold had the rows written in order); the slot is then never
 // a source, so no row of the group reads it.
+template <bool GROUPED = true>
 __device__ __forceinline__ bool writes_slot(const Params& p, int64_t t) {
   if (p.write_idx < 0) return false;
-  if (p.bank_group == 1) return true;
+  if (!GROUPED || p.bank_group == 1) return true;
   return ((uint32_t)t % (uint32_t)p.bank_group) == (uint32_t)(p.bank_group - 1) || t == p.tokens - 1;
 }
 

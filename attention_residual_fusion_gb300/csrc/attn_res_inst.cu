@@ -39,13 +39,14 @@ StreamLaunchFn pick_stream(bool d, bool o) {
   constexpr int K = kStreamShapes[SH].k;
   constexpr int V = kStreamShapes[SH].vpt;
   constexpr int ST = kStreamShapes[SH].stages;
-  if (d) return o ? &launch_stream<S, true, true, K, V, ST> : &launch_stream<S, true, false, K, V, ST>;
-  return o ? &launch_stream<S, false, true, K, V, ST> : &launch_stream<S, false, false, K, V, ST>;
+  constexpr bool G = kStreamShapes[SH].grouped;
+  if (d) return o ? &launch_stream<S, true, true, K, V, ST, G> : &launch_stream<S, true, false, K, V, ST, G>;
+  return o ? &launch_stream<S, false, true, K, V, ST, G> : &launch_stream<S, false, false, K, V, ST, G>;
 }
 }  // namespace
 
 StreamLaunchFn ATTN_RES_CAT(stream_launcher_s, ATTN_RES_S)(int shape_idx, bool d, bool o) {
-  static_assert(kNumStreamShapes == 8, "update the switch below");
+  static_assert(kNumStreamShapes == 9, "update the switch below");
   switch (shape_idx) {
     case 0: return pick_stream<0>(d, o);
     case 1: return pick_stream<1>(d, o);
@@ -55,6 +56,7 @@ StreamLaunchFn ATTN_RES_CAT(stream_launcher_s, ATTN_RES_S)(int shape_idx, bool d
     case 5: return pick_stream<5>(d, o);
     case 6: return pick_stream<6>(d, o);
     case 7: return pick_stream<7>(d, o);
+    case 8: return pick_stream<8>(d, o);
     default: return nullptr;
   }
 }

@@ -72,14 +72,19 @@ cudaError_t launch_split(const Params& p, int64_t T, bool pdl,
 // 16-byte vectors per thread and per row (VPT), ring depth (STAGES).
 struct StreamShape {
   int k, vpt, stages;
+  bool grouped;  // built for B > 1 token rows per bank row
 };
-constexpr StreamShape kStreamShapes[] = {{7, 1, 2}, {7, 2, 2}, {7, 2, 3}, {7, 4, 2},
-                                         {4, 2, 2}, {4, 2, 3}, {14, 1, 2}, {14, 2, 2}};
+// The last entry is the one shape built for shared bank rows (B > 1).
+constexpr StreamShape kStreamShapes[] = {{7, 1, 2, false}, {7, 2, 2, false}, {7, 2, 3, false},
+                                         {7, 4, 2, false}, {4, 2, 2, false}, {4, 2, 3, false},
+                                         {14, 1, 2, false}, {14, 2, 2, false}, {7, 2, 2, true}};
 constexpr int kNumStreamShapes = sizeof(kStreamShapes) / sizeof(kStreamShapes[0]);
+constexpr int kGroupedStreamShape = kNumStreamShapes - 1;
 
-inline int stream_shape_index(int k, int vpt, int stages) {
+inline int stream_shape_index(int k, int vpt, int stages, bool grouped) {
   for (int i = 0; i < kNumStreamShapes; ++i)
-    if (kStreamShapes[i].k == k && kStreamShapes[i].vpt == vpt && kStreamShapes[i].stages == stages)
+    if (kStreamShapes[i].k == k && kStreamShapes[i].vpt == vpt &&
+        kStreamShapes[i].stages == stages && kStreamShapes[i].grouped == grouped)
       return i;
   return -1;
 }
@@ -89,11 +94,11 @@ inline int stream_shape_index(int k, int vpt, int stages) {
 using StreamLaunchFn = cudaError_t (*)(const Params&, int64_t T, bool pdl,
                                        cudaStream_t stream, int device);
 
-template <int S, bool D, bool O, int K, int VPT, int STAGES>
+template <int S, bool D, bool O, int K, int VPT, int STAGES, bool G>
 cudaError_t launch_stream(const Params& p, int64_t T, bool pdl, cudaStream_t stream,
                           int device) {
   using C = attn_res_dev::StreamCfg<S, D, O, K, VPT, STAGES>;
-  void (*kern)(Params, int64_t) = attn_res_dev::attn_res_stream_kernel<S, D, O, K, VPT, STAGES>;
+  void (*kern)(Params, int64_t) = attn_res_dev::attn_res_stream_kernel<S, D, O, K, VPT, STAGES, G>;
   // per device: attributes set and the number of co-resident clusters
   static std::atomic<int> clusters_per_device[64];
   if (device < 0 || device >= 64) return cudaErrorInvalidDevice;

@@ -65,7 +65,9 @@ struct StreamCfg {
   static_assert(STAGES >= 2 && STAGES <= 4, "ring depth");
 };
 
-template <int S, bool HAS_DELTA, bool HAS_ONORM, int K, int VPT, int STAGES>
+// GROUPED: B token rows per bank row with B > 1 possible (else B == 1 and the
+// token loop carries no test for it).
+template <int S, bool HAS_DELTA, bool HAS_ONORM, int K, int VPT, int STAGES, bool GROUPED>
 __global__ void __launch_bounds__(StreamCfg<S, HAS_DELTA, HAS_ONORM, K, VPT, STAGES>::THREADS,
                                   StreamCfg<S, HAS_DELTA, HAS_ONORM, K, VPT, STAGES>::MIN_BLOCKS)
     attn_res_stream_kernel(const Params p, const int64_t T) {
@@ -124,7 +126,7 @@ __global__ void __launch_bounds__(StreamCfg<S, HAS_DELTA, HAS_ONORM, K, VPT, STA
     __syncwarp();
     if (lane < S)
       bulk_load(ring_addr + (uint32_t)(s * S + lane) * C::SLICE_BYTES,
-                bank_of(p, t) + slice0 + (int64_t)lane * p.blocks_slot,
+                bank_of<GROUPED>(p, t) + slice0 + (int64_t)lane * p.blocks_slot,
                 C::SLICE_BYTES, bar);
   };
   // every thread: its vectors of the token's prefix and delta rows
@@ -238,8 +240,8 @@ __global__ void __launch_bounds__(StreamCfg<S, HAS_DELTA, HAS_ONORM, K, VPT, STA
     if (j + 1 < ntok) phase_a(j + 1, c_next);
 
     // C(j): output norm and stores
-    const bool slot_write = writes_slot(p, t);
-    uint16_t* const slot = const_cast<uint16_t*>(bank_of(p, t)) + (int64_t)p.write_idx * p.blocks_slot;
+    const bool slot_write = writes_slot<GROUPED>(p, t);
+    uint16_t* const slot = const_cast<uint16_t*>(bank_of<GROUPED>(p, t)) + (int64_t)p.write_idx * p.blocks_slot;
     uint4 o[VPT];
     token_finish<S, HAS_DELTA, HAS_ONORM, K, NW, VPT>(mb, b, bparity, lane, p.out_eps, failed,
                                                        p.err, ow, acc, o);

@@ -117,7 +117,9 @@ typedef struct {
  * in token order would leave), and only that row writes it.  Because the
  * other rows of the group would read a slot that is being written,
  * 0 <= block_write_idx < num_blocks is ATTN_RES_EINVAL when B > 1; a
- * negative blocks_group is ATTN_RES_EINVAL too. */
+ * negative blocks_group is ATTN_RES_EINVAL too.  With B > 1 the stream
+ * kernel is built in one shape, (7,2,2); other stream overrides are
+ * ATTN_RES_EINVAL. */
 
 /*
  * attn_res -- enqueue the AttnRes mixture for T token rows on `stream`.

@@ -346,3 +346,12 @@ def test_shared_bank_rows_host_checks(lib):
         assert call(**kw) in (4, 5)
     kw["layout"].blocks_group = 1                        # four bank rows: overlaps
     assert call(**kw) == 3
+    # B > 1: the stream kernel has the one shape (7,2,2)
+    kw = good(T=300, S=4, widx=6)
+    kw["layout"].blocks_group = 2
+    kw["layout"].blocks_token = 8 * H
+    kw["layout"].flags = ar.FLAG_KERNEL(2) | ar.FLAG_VPT(4)
+    assert call(**kw) == 1
+    kw["layout"].flags = ar.FLAG_KERNEL(2) | ar.FLAG_SPLIT(7) | ar.FLAG_VPT(2) | ar.FLAG_STAGES(2)
+    if no_gpu:
+        assert call(**kw) in (4, 5)
