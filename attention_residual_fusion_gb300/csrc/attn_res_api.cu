@@ -41,10 +41,14 @@ struct Plan {
 //  * few tokens (T < 128), or no exchange at all (no bank rows and no output
 //    norm): the split kernel, 7 CTAs x 128 threads per token, all threads
 //    active, so a token's latency chain runs on 7 SMs at once;
-//  * otherwise the stream kernel: persistent clusters of 7 CTAs and a 2-deep
-//    TMA ring, with 4 vectors per thread (one warp per CTA, fewer warps and so
-//    less reduction and exchange work per token) when there are 6 or more bank
-//    rows or an output norm, else 2 vectors per thread (more warps per SM).
+//  * otherwise the stream kernel, persistent clusters with a 2-deep TMA ring,
+//    shape (CTAs per token, vectors per thread, stages):
+//      (7,4,2) with 1..5 bank rows and an output norm: one warp per CTA, so
+//              fewer warps share the reduction and exchange work of a token;
+//      (4,2,2) with no bank rows (output norm only): 4 CTAs per token, so a
+//              token's short exchange spans fewer CTAs;
+//      (7,2,2) otherwise (6..8 bank rows, or no output norm): two warps per
+//              CTA, more warps per SM to cover the longer per-token work.
 //  * with shared bank rows (B > 1) the stream kernel has one shape, (7,2,2).
 attn_res_status_t make_plan(int64_t T, int num_blocks, bool has_onorm, uint32_t flags, bool grouped,
                             Plan* out) {
@@ -66,9 +70,11 @@ attn_res_status_t make_plan(int64_t T, int num_blocks, bool has_onorm, uint32_t 
     if (pl.split != 0 || pl.stages != 0 || pl.vpt != 0) return ATTN_RES_EINVAL;
     pl.split = 1;
   } else if (pl.kernel == ATTN_RES_KERNEL_STREAM) {
-    if (pl.split == 0) pl.split = 7;
+    if (pl.split == 0)
+      pl.split = (!grouped && num_blocks == 0 && (pl.vpt == 0 || pl.vpt == 2)) ? 4 : 7;
     if (pl.stages == 0) pl.stages = 2;
-    if (pl.vpt == 0) pl.vpt = (!grouped && pl.split == 7 && (num_blocks >= 6 || has_onorm)) ? 4 : 2;
+    if (pl.vpt == 0)
+      pl.vpt = (!grouped && pl.split == 7 && num_blocks >= 1 && num_blocks <= 5 && has_onorm) ? 4 : 2;
     pl.shape = stream_shape_index(pl.split, pl.vpt, pl.stages, grouped);
     if (pl.shape < 0) return ATTN_RES_EINVAL;
   } else {

@@ -96,9 +96,22 @@ def measured_peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
-def recorded_traffic(workload: str):
+def kernel_label(wl, shape) -> str:
+    """The timed kernel as ncu names it (template arguments of the launch)."""
+    d, o = int(wl.delta is not None), int(wl.out_norm_w is not None)
+    if shape["kernel"] == "stream":
+        vpt = {(7, 32): 4, (7, 64): 2, (7, 128): 1, (4, 128): 2, (14, 32): 2, (14, 64): 1}
+        v = vpt.get((shape["split"], shape["threads"]), 0)
+        return (f"attn_res_stream_kernel<{wl.num_blocks},{d},{o},{shape['split']},{v},"
+                f"{shape['stages']},{int(wl.group > 1)}>")
+    if shape["kernel"] == "split":
+        return f"attn_res_split_kernel<{wl.num_blocks},{d},{o},{shape['split']}>"
+    return f"attn_res_{shape['kernel']}_kernel<{wl.num_blocks},{d},{o}>"
+
+
+def recorded_traffic(workload: str, kernel: str):
     """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current kernel source and this workload."""
+    on the current kernel source, this workload and this kernel variant."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
@@ -107,7 +120,7 @@ def recorded_traffic(workload: str):
     except Exception:
         return None
     e = d.get(workload)
-    if not e or e.get("source_digest") != source_digest():
+    if not e or e.get("source_digest") != source_digest() or e.get("kernel") != kernel:
         return None
     return e.get("dram_bytes_per_launch")
 
@@ -564,8 +577,8 @@ def run_ours(args, rank, world, local_rank, dist):
                      "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs, copy)",
                      "algorithmic_bytes_per_launch": alg_bytes,
                      "mean_launch_us": round(mean_launch_ms * 1e3, 3),
-                     "traffic": recorded_traffic(args.workload),
-                     "kernel": f"attn_res_{shape['kernel']}_kernel"},
+                     "traffic": recorded_traffic(args.workload, kernel_label(wl, shape)),
+                     "kernel": kernel_label(wl, shape)},
         "gpu_launches": args.steps,
         "clocks": clk.summary(),
     }

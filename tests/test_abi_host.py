@@ -45,9 +45,12 @@ def test_launch_shape(lib):
     ls = ar.launch_shape
     assert ls(1, 4, True) == dict(kernel="split", split=7, stages=0, threads=128, ctas=7, cluster=7)
     assert ls(64, 8, False) == dict(kernel="split", split=7, stages=0, threads=128, ctas=448, cluster=7)
-    assert ls(8192, 8, True) == dict(kernel="stream", split=7, stages=2, threads=32, ctas=0, cluster=7)
+    assert ls(8192, 8, True) == dict(kernel="stream", split=7, stages=2, threads=64, ctas=0, cluster=7)
+    assert ls(8192, 4, True) == dict(kernel="stream", split=7, stages=2, threads=32, ctas=0, cluster=7)
     assert ls(8192, 4, False) == dict(kernel="stream", split=7, stages=2, threads=64, ctas=0, cluster=7)
-    assert ls(8192, 0, True)["threads"] == 32
+    assert ls(8192, 0, True) == dict(kernel="stream", split=4, stages=2, threads=128, ctas=0, cluster=4)
+    assert ls(8192, 0, True, ar.FLAG_VPT(4))["split"] == 7
+    assert ls(8192, 0, True, ar.FLAG_STAGES(3))["split"] == 4
     # no softmax and no output norm: the CTAs of a token never talk
     assert ls(1024, 0, False) == dict(kernel="split", split=7, stages=0, threads=128, ctas=7168, cluster=1)
     assert ls(2, 8, True, ar.FLAG_SPLIT(16)) == dict(kernel="split", split=16, stages=0, threads=64, ctas=32, cluster=16)
