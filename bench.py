@@ -577,6 +577,8 @@ def run_ours(args, rank, world, local_rank, dist):
                      "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs, copy)",
                      "algorithmic_bytes_per_launch": alg_bytes,
                      "mean_launch_us": round(mean_launch_ms * 1e3, 3),
+                     "launch_us_p20_p50_p80": [round(float(np.percentile(per, q)) * 1e3, 3)
+                                               for q in (20, 50, 80)],
                      "traffic": recorded_traffic(args.workload, kernel_label(wl, shape)),
                      "kernel": kernel_label(wl, shape)},
         "gpu_launches": args.steps,
