@@ -117,7 +117,22 @@ def attn_res_tp(prefix, delta, blocks, num_blocks: int, block_write_idx: int, re
     float32 tensor in place over the ranks (default torch.distributed's
     all_reduce on ``group``; with no process group initialised the call is
     local).  ``gram`` selects the single-exchange form; ``blocks_group`` as
-    for attn_res.  Returns ``out`` (allocated if not given)."""
+    for attn_res.  With ``stream`` given, the buffers, the kernels and the
+    all-reduces are all ordered on that stream.  Returns ``out`` (allocated
+    if not given)."""
+    import contextlib
+
+    import torch
+
+    ctx = torch.cuda.stream(stream) if stream is not None else contextlib.nullcontext()
+    with ctx:
+        return _attn_res_tp(prefix, delta, blocks, num_blocks, block_write_idx, res_w, rms_w,
+                            out_norm_w, eps, out_eps, out, H, group, all_reduce, phases, gram,
+                            pdl, blocks_group, stream)
+
+
+def _attn_res_tp(prefix, delta, blocks, num_blocks, block_write_idx, res_w, rms_w, out_norm_w,
+                 eps, out_eps, out, H, group, all_reduce, phases, gram, pdl, blocks_group, stream):
     import torch
     import torch.distributed as dist
 
