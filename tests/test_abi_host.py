@@ -358,3 +358,27 @@ def test_shared_bank_rows_host_checks(lib):
     kw["layout"].flags = ar.FLAG_KERNEL(2) | ar.FLAG_SPLIT(7) | ar.FLAG_VPT(2) | ar.FLAG_STAGES(2)
     if no_gpu:
         assert call(**kw) in (4, 5)
+
+
+def test_binding_rejects_host_tensors_and_bad_shapes(lib):
+    """The binding only marshals device bf16 tensors: host or float tensors,
+    and a bank with fewer than ceil(T / blocks_group) token rows, are refused
+    before any call (no CPU path)."""
+    import torch
+    from attention_residual_fusion_gb300 import tp
+    T, Hh = 4, 64
+    p = torch.zeros((T, Hh), dtype=torch.bfloat16)
+    b = torch.zeros((T, 8, Hh), dtype=torch.bfloat16)
+    w = torch.ones(Hh, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        ar.attn_res(p, None, b, 4, -1, w, w)                      # host tensors
+    with pytest.raises(ValueError):
+        ar.attn_res(p.float(), None, b, 4, -1, w, w)              # not bf16
+    with pytest.raises(ValueError):
+        tp.tp_sums(p, None, b, 4, w, w, torch.zeros((T, 10)))     # host tensors
+    with pytest.raises(ValueError):
+        ar.make_layout(p, None, b[:1], None, 0, blocks_group=2)   # 1 < ceil(4 / 2) bank rows
+    lay = ar.make_layout(p, None, b[:2], None, 0, blocks_group=2)
+    assert lay.blocks_group == 2 and lay.blocks_token == 8 * Hh and lay.blocks_capacity == 8
+    with pytest.raises(ValueError):
+        ar.make_layout(p, None, b.transpose(1, 2), None, 0)       # inner stride not 1

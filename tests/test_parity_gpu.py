@@ -325,3 +325,34 @@ def test_shared_bank_rows_reject_written_source():
     with pytest.raises(ar.AttnResError) as e:
         G.run_gpu(wl)
     assert e.value.status == 1
+
+
+def _nan_equal(a, b):
+    """Bit-equal, except that any NaN pattern matches any NaN pattern."""
+    fa, fb = R.widen(a), R.widen(b)
+    both_nan = np.isnan(fa) & np.isnan(fb)
+    return bool(np.all((a == b) | both_nan))
+
+
+@pytest.mark.parametrize("kernel", [ar.KERNEL_SPLIT, ar.KERNEL_STREAM, ar.KERNEL_GENERIC])
+def test_nonfinite_inputs_stay_in_their_token(kernel):
+    """A NaN or an infinity in one token's rows makes that token's output NaN
+    (IEEE arithmetic, as in the oracle) and leaves every other token as the
+    oracle computes it; write-backs stay exact (NaN for NaN)."""
+    wl = W.make_workload(37, 8, capacity=9, has_delta=True, has_out_norm=True,
+                         block_write_idx=8, seed=44, mixing=True)
+    nan, inf = np.uint16(0x7FC0), np.uint16(0x7F80)
+    wl.bank[3, 2, 100] = nan          # a bank row of token 3
+    wl.bank[7, 5, 50] = inf           # an infinite bank element of token 7
+    wl.delta[11, 4000] = nan          # c of token 11 is NaN in one column
+    wl.prefix[20, 7] = inf            # c of token 20 is infinite in one column
+    ref = oracle.run_workload(wl, n_threads=NT)
+    gpu = G.run_gpu(wl, kernel=kernel)
+    bad = [3, 7, 11, 20]
+    rest = np.array([t for t in range(wl.T) if t not in bad])
+    G.assert_out_close(gpu["out"][rest], ref["out"][rest], "finite tokens")
+    for t in bad:
+        assert np.all(np.isnan(R.widen(ref["out"][t]))), t
+        assert np.all(np.isnan(R.widen(gpu["out"][t]))), t
+    assert _nan_equal(gpu["prefix"], ref["prefix"][:, :wl.H])
+    assert _nan_equal(gpu["bank"], ref["bank"])
