@@ -241,7 +241,9 @@ __global__ void __launch_bounds__(StreamCfg<S, HAS_DELTA, HAS_ONORM, K, VPT, STA
 
     // C(j): output norm and stores
     const bool slot_write = writes_slot<GROUPED>(p, t);
-    uint16_t* const slot = const_cast<uint16_t*>(bank_of<GROUPED>(p, t)) + (int64_t)p.write_idx * p.blocks_slot;
+    uint16_t* const slot = slot_write ? const_cast<uint16_t*>(bank_of<GROUPED>(p, t)) +
+                                            (int64_t)p.write_idx * p.blocks_slot
+                                      : nullptr;
     uint4 o[VPT];
     token_finish<S, HAS_DELTA, HAS_ONORM, K, NW, VPT>(mb, b, bparity, lane, p.out_eps, failed,
                                                        p.err, ow, acc, o);
