@@ -45,8 +45,8 @@ struct Plan {
 //    shape (CTAs per token, vectors per thread, stages):
 //      (7,4,2) with 1..5 bank rows and an output norm: one warp per CTA, so
 //              fewer warps share the reduction and exchange work of a token;
-//      (4,2,2) with no bank rows (output norm only): 4 CTAs per token, so a
-//              token's short exchange spans fewer CTAs;
+//      (2,4,2) with no bank rows (output norm only): 2 CTAs of 4 warps per
+//              token, so a token's short exchange spans only two CTAs;
 //      (7,2,2) otherwise (6..8 bank rows, or no output norm): two warps per
 //              CTA, more warps per SM to cover the longer per-token work.
 //  * with shared bank rows (B > 1) the stream kernel has one shape, (7,2,2).
@@ -70,11 +70,17 @@ attn_res_status_t make_plan(int64_t T, int num_blocks, bool has_onorm, uint32_t 
     if (pl.split != 0 || pl.stages != 0 || pl.vpt != 0) return ATTN_RES_EINVAL;
     pl.split = 1;
   } else if (pl.kernel == ATTN_RES_KERNEL_STREAM) {
-    if (pl.split == 0)
-      pl.split = (!grouped && num_blocks == 0 && (pl.vpt == 0 || pl.vpt == 2)) ? 4 : 7;
+    const bool no_bank = !grouped && num_blocks == 0;
+    if (pl.split == 0) {
+      pl.split = 7;
+      if (no_bank && (pl.vpt == 0 || pl.vpt == 4)) pl.split = 2;
+      if (no_bank && pl.vpt == 2) pl.split = 4;
+    }
     if (pl.stages == 0) pl.stages = 2;
-    if (pl.vpt == 0)
-      pl.vpt = (!grouped && pl.split == 7 && num_blocks >= 1 && num_blocks <= 5 && has_onorm) ? 4 : 2;
+    if (pl.vpt == 0) {
+      const bool one_warp = pl.split == 7 && num_blocks >= 1 && num_blocks <= 5 && has_onorm;
+      pl.vpt = (!grouped && (one_warp || pl.split == 2)) ? 4 : 2;
+    }
     pl.shape = stream_shape_index(pl.split, pl.vpt, pl.stages, grouped);
     if (pl.shape < 0) return ATTN_RES_EINVAL;
   } else {

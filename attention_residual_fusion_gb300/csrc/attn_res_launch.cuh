@@ -77,7 +77,7 @@ struct StreamShape {
 // The last entry is the one shape built for shared bank rows (B > 1).
 constexpr StreamShape kStreamShapes[] = {{7, 1, 2, false}, {7, 2, 2, false}, {7, 2, 3, false},
                                          {7, 4, 2, false}, {4, 2, 2, false}, {4, 2, 3, false},
-                                         {14, 1, 2, false}, {14, 2, 2, false}, {7, 2, 2, true}};
+                                         {2, 4, 2, false}, {14, 2, 2, false}, {7, 2, 2, true}};
 constexpr int kNumStreamShapes = sizeof(kStreamShapes) / sizeof(kStreamShapes[0]);
 constexpr int kGroupedStreamShape = kNumStreamShapes - 1;
 

@@ -48,9 +48,13 @@ def test_launch_shape(lib):
     assert ls(8192, 8, True) == dict(kernel="stream", split=7, stages=2, threads=64, ctas=0, cluster=7)
     assert ls(8192, 4, True) == dict(kernel="stream", split=7, stages=2, threads=32, ctas=0, cluster=7)
     assert ls(8192, 4, False) == dict(kernel="stream", split=7, stages=2, threads=64, ctas=0, cluster=7)
-    assert ls(8192, 0, True) == dict(kernel="stream", split=4, stages=2, threads=128, ctas=0, cluster=4)
-    assert ls(8192, 0, True, ar.FLAG_VPT(4))["split"] == 7
-    assert ls(8192, 0, True, ar.FLAG_STAGES(3))["split"] == 4
+    assert ls(8192, 0, True) == dict(kernel="stream", split=2, stages=2, threads=128, ctas=0, cluster=2)
+    assert ls(8192, 0, True, ar.FLAG_VPT(2))["split"] == 4
+    assert ls(8192, 0, True, ar.FLAG_VPT(1))["split"] == 7
+    assert ls(8192, 0, True, ar.FLAG_VPT(2) | ar.FLAG_STAGES(3))["split"] == 4
+    with pytest.raises(ar.AttnResError):
+        ls(8192, 0, True, ar.FLAG_STAGES(3))          # (2,4,3) is not built
+    assert ls(9000, 0, True, ar.FLAG_SPLIT(2))["threads"] == 128
     # no softmax and no output norm: the CTAs of a token never talk
     assert ls(1024, 0, False) == dict(kernel="split", split=7, stages=0, threads=128, ctas=7168, cluster=1)
     assert ls(2, 8, True, ar.FLAG_SPLIT(16)) == dict(kernel="split", split=16, stages=0, threads=64, ctas=32, cluster=16)
@@ -66,6 +70,7 @@ def test_launch_shape(lib):
                 (1, 1, 0, ar.FLAG_KERNEL(3) | ar.FLAG_SPLIT(7)),
                 (1, 1, 0, ar.FLAG_KERNEL(2) | ar.FLAG_STAGES(4)),
                 (1, 1, 0, ar.FLAG_KERNEL(2) | ar.FLAG_SPLIT(8) | ar.FLAG_VPT(2)),
+                (1, 1, 0, ar.FLAG_KERNEL(2) | ar.FLAG_SPLIT(14) | ar.FLAG_VPT(1)),
                 (1, 1, 0, ar.FLAG_KERNEL(2) | ar.FLAG_STAGES(4)),
                 (1, 1, 0, ar.FLAG_KERNEL(2) | ar.FLAG_SPLIT(7) | ar.FLAG_VPT(1) | ar.FLAG_STAGES(3)),
                 (1, 1, 0, ar.FLAG_KERNEL(1) | ar.FLAG_VPT(2)),
