@@ -26,7 +26,7 @@ constexpr uint32_t kKnownFlags = ATTN_RES_FLAG_PDL | ATTN_RES_FLAG_SPLIT(0xff) |
                                  ATTN_RES_FLAG_VPT(0xf);
 
 // From this many tokens on, the persistent stream kernel is used.
-constexpr int64_t kStreamMinTokens = 128;
+constexpr int64_t kStreamMinTokens = 80;
 
 struct Plan {
   int kernel;  // ATTN_RES_KERNEL_SPLIT or ATTN_RES_KERNEL_STREAM
@@ -38,7 +38,8 @@ struct Plan {
 
 // Automatic choice (measured on GB300 over the prefill, decode and long
 // prefill workloads):
-//  * few tokens (T < 128), or no exchange at all (no bank rows and no output
+//  * few tokens (T < 80: split 5.2 µs vs stream 6.0 µs at T = 64, 8.7 vs 7.6
+//    µs at T = 96, 8 bank rows), or no exchange at all (no bank rows and no output
 //    norm): the split kernel, 7 CTAs x 128 threads per token, all threads
 //    active, so a token's latency chain runs on 7 SMs at once;
 //  * otherwise the stream kernel, persistent clusters with a 2-deep TMA ring,

@@ -84,7 +84,7 @@ typedef enum {
  * no bank rows (4 if VPT 2 is given, 7 for another VPT), else 7; stages 2;
  * VPT 4 with split 2, or with split 7, 1..5 bank rows and an output norm,
  * else 2 -- so (7,4,2), (2,4,2) with no bank rows, and (7,2,2) otherwise.
- * The kernel defaults to the split kernel below 128 tokens and when there is
+ * The kernel defaults to the split kernel below 80 tokens and when there is
  * neither a bank row nor an output norm, else the stream kernel. */
 #define ATTN_RES_FLAG_SPLIT(k) (((uint32_t)(k) & 0xffu) << 8)
 #define ATTN_RES_FLAG_KERNEL(k) (((uint32_t)(k) & 0xfu) << 16)
