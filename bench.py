@@ -20,6 +20,8 @@ than L2, so no flush is needed between steps.
              dependent launch (T=1 and T=1024)
   prefill_cells  T=1024/2048 prefill cells: µs per call from CUDA-graph
              replay, cycling through input copies larger than 3x L2
+  width_cells  other model widths (H = 4096, 8192) through attn_res_h and
+             the general kernel, graph replay over rotating input sets
   tp_cells   one rank's kernels of the hidden-sharded (TP8) mixture, both
              exchange forms, all-reduces excluded
   cpu_baseline  the CPU oracle on a bounded sample of the same workload
@@ -68,6 +70,12 @@ def make(name: str):
     if kind == "decode":           # decode:T
         T = int(a[0])
         return W.decode_batch(T), f"decode batch T={T}, S=8, delta, output norm, per-block scales U(0.5,20)"
+    if kind == "width":            # width:H:T:S -- another model width (general kernel)
+        H, T, S = (int(x) for x in a)
+        return (W.make_workload(T, S, capacity=8, has_delta=True, has_out_norm=True,
+                                block_write_idx=7, seed=0, outliers=True, H=H,
+                                name=f"width_H{H}_T{T}_S{S}"),
+                f"hidden size H={H}, T={T}, S={S}, delta, output norm, write_idx 7, 1% outliers x50")
     if kind == "variant":          # variant:T:S:d:o:w
         T, S, d, o, w = (int(x) for x in a)
         return W.variant_cell(T, S, bool(d), bool(o), w), f"variant T={T}, S={S}, delta {bool(d)}, output norm {bool(o)}, write_idx {w}"
@@ -322,6 +330,27 @@ def sweep_prefill(ar, torch, dev, stream, peak):
                      "tokens_per_s": round(wl.T / (us * 1e-6), 1),
                      "gbs": round(gbs, 1), "frac": round(gbs / peak, 4),
                      "input_sets": len(sets)})
+        del t, sets
+        torch.cuda.empty_cache()
+    return rows
+
+
+WIDTHS = ["width:4096:2048:8", "width:8192:2048:8"]
+
+
+def width_cells(ar, torch, dev, stream, peak):
+    """Other model widths (the general kernel behind attn_res_h): µs per call
+    from graph replay over rotating input sets larger than 3x L2."""
+    rows = []
+    for name in WIDTHS:
+        wl, _ = make(name)
+        t = device_tensors(wl, torch, dev)
+        sets = input_sets(wl, t, torch, dev)
+        us = time_graph(ar, wl, sets, torch, stream)
+        gbs = wl.algorithmic_bytes() / (us * 1e-6) / 1e9
+        rows.append({"workload": name, "kernel": "general", "us_per_call": round(us, 2),
+                     "tokens_per_s": round(wl.T / (us * 1e-6), 1), "gbs": round(gbs, 1),
+                     "frac": round(gbs / peak, 4), "input_sets": len(sets)})
         del t, sets
         torch.cuda.empty_cache()
     return rows
@@ -593,6 +622,10 @@ def run_ours(args, rank, world, local_rank, dist):
         torch.cuda.empty_cache()
         line["prefill_cells"] = sweep_prefill(ar, torch, dev, stream, peak)
         t = None
+    if rank == 0 and not args.no_sweep:
+        t = None
+        torch.cuda.empty_cache()
+        line["width_cells"] = width_cells(ar, torch, dev, stream, peak)
     if rank == 0 and not args.no_tp:
         t = None
         torch.cuda.empty_cache()
