@@ -332,6 +332,7 @@ attn_res_status_t check_rows(const RowArgs& a, Params* p) {
   p->write_idx = a.writes ? a.write_idx : -1;
   p->bank_group = group;
   p->tokens = T;
+  p->inv_h = 1.0f / static_cast<float>(H);
   p->err = nullptr;
   return ATTN_RES_OK;
 }
@@ -369,12 +370,29 @@ attn_res_status_t run(int64_t H, attn_res_bf16_t* prefix, const attn_res_bf16_t*
   if (make_plan(T, num_blocks, out_norm_w != nullptr, layout->flags, bank_group(layout) > 1,
                 &plan) != ATTN_RES_OK)
     return ATTN_RES_EINVAL;
-  // widths other than the one the fast kernels are built for take the
-  // general kernel
+  // other widths: the stream kernel's any-width form when H is a multiple
+  // of 1024 (at most 16 CTAs per row) and the call would stream, else the
+  // general kernel; no shape overrides
   if (H != kH) {
-    const int forced = static_cast<int>((layout->flags >> 16) & 0xfu);
-    if (forced != 0 && forced != ATTN_RES_KERNEL_GENERIC) return ATTN_RES_EINVAL;
-    plan.kernel = ATTN_RES_KERNEL_GENERIC;
+    const uint32_t f = layout->flags;
+    const int forced = static_cast<int>((f >> 16) & 0xfu);
+    const bool overrides = ((f >> 8) & 0xffu) != 0 || ((f >> 20) & 0xffu) != 0;
+    const bool any_width = H % attn_res_dev::kRtCols == 0 &&
+                           H / attn_res_dev::kRtCols <= attn_res_dev::kRtMaxK;
+    const bool exchange = num_blocks > 0 || out_norm_w != nullptr;
+    if (forced == ATTN_RES_KERNEL_SPLIT) return ATTN_RES_EINVAL;
+    if (forced == ATTN_RES_KERNEL_STREAM && (!any_width || overrides || !exchange))
+      return ATTN_RES_EINVAL;
+    const bool stream_it = forced == ATTN_RES_KERNEL_STREAM ||
+                           (forced == 0 && !overrides && any_width && exchange &&
+                            T >= kStreamMinTokens);
+    if (stream_it) {
+      plan.kernel = ATTN_RES_KERNEL_STREAM;
+      plan.shape = kAnyWidthStreamShape;
+      plan.split = static_cast<int>(H / attn_res_dev::kRtCols);
+    } else {
+      plan.kernel = ATTN_RES_KERNEL_GENERIC;
+    }
   }
   if (plan.kernel == ATTN_RES_KERNEL_GENERIC) plan.split = 1;
   if (T * plan.split > INT32_MAX) return ATTN_RES_EINVAL;
@@ -420,7 +438,7 @@ attn_res_status_t run(int64_t H, attn_res_bf16_t* prefix, const attn_res_bf16_t*
     } else {
       StreamLaunchFn fn = lookup_stream(num_blocks, plan.shape, has_delta, has_onorm);
       if (fn == nullptr) return ATTN_RES_EINVAL;
-      e = fn(p, T, pdl, static_cast<cudaStream_t>(stream), dev);
+      e = fn(p, T, pdl, static_cast<cudaStream_t>(stream), dev, plan.split);
     }
   }
   if (e != cudaSuccess) {

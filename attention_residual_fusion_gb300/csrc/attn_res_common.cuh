@@ -23,6 +23,7 @@ struct Params {
   uint16_t* out;
   int64_t prefix_row, delta_row, blocks_token, blocks_slot, out_row;
   int64_t bank_group;  // B: token rows per bank row (>= 1)
+  float inv_h;         // 1 / H (the kernels built for H = 7168 use a constant)
   int64_t tokens;      // T
   int write_idx;
   float eps, out_eps;
@@ -95,6 +96,11 @@ __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
   return r;
+}
+__device__ __forceinline__ uint32_t cluster_nctarank() {
+  uint32_t n;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(n));
+  return n;
 }
 __device__ __forceinline__ void cluster_arrive_release() {
   asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");

@@ -62,7 +62,7 @@ __global__ void __launch_bounds__(SplitCfg<S, HAS_DELTA, HAS_ONORM, K>::THREADS)
     if (tid == 0) {
       mailbox_init(mb);
       fence_mbar_init();
-      mailbox_expect<Tok>(mb, 0, HAS_ONORM);
+      mailbox_expect<Tok>(mb, 0, HAS_ONORM, Split{K, kInvH});
     }
     // Announce this CTA (and its initialised mailboxes) to the cluster; the
     // matching wait, just before the first remote store, guarantees every
@@ -105,7 +105,7 @@ __global__ void __launch_bounds__(SplitCfg<S, HAS_DELTA, HAS_ONORM, K>::THREADS)
   }
   mix_token<S, HAS_DELTA, HAS_ONORM, K, C::NW, 1>(
       [&](int i, int) { return x[i]; }, q, owv, mb, 0, 0u, rank, warp, lane, p.eps, p.out_eps,
-      failed, p.err, [] {}, c, o);
+      failed, p.err, [] {}, c, o, Split{K, kInvH});
 
   // 4. stores; the write-backs follow every read of this column slice
   if (active) {

@@ -74,12 +74,17 @@ struct StreamShape {
   int k, vpt, stages;
   bool grouped;  // built for B > 1 token rows per bank row
 };
-// The last entry is the one shape built for shared bank rows (B > 1).
+// The next-to-last entry is the one shape built for shared bank rows (B > 1);
+// the last (k = 0) serves any width H that is a multiple of 1024: H / 1024
+// CTAs per token row, each with the per-CTA layout of (7,2,2), shared bank
+// rows allowed.
 constexpr StreamShape kStreamShapes[] = {{7, 1, 2, false}, {7, 2, 2, false}, {7, 2, 3, false},
                                          {7, 4, 2, false}, {4, 2, 2, false}, {4, 2, 3, false},
-                                         {2, 4, 2, false}, {14, 2, 2, false}, {7, 2, 2, true}};
+                                         {2, 4, 2, false}, {14, 2, 2, false}, {7, 2, 2, true},
+                                         {0, 2, 2, true}};
 constexpr int kNumStreamShapes = sizeof(kStreamShapes) / sizeof(kStreamShapes[0]);
-constexpr int kGroupedStreamShape = kNumStreamShapes - 1;
+constexpr int kGroupedStreamShape = kNumStreamShapes - 2;
+constexpr int kAnyWidthStreamShape = kNumStreamShapes - 1;
 
 inline int stream_shape_index(int k, int vpt, int stages, bool grouped) {
   for (int i = 0; i < kNumStreamShapes; ++i)
@@ -92,33 +97,36 @@ inline int stream_shape_index(int k, int vpt, int stages, bool grouped) {
 // Enqueue the persistent kernel: as many clusters as fit on the device at
 // once (at most T), each streaming every ncl-th token.
 using StreamLaunchFn = cudaError_t (*)(const Params&, int64_t T, bool pdl,
-                                       cudaStream_t stream, int device);
+                                       cudaStream_t stream, int device, int kc);
 
 template <int S, bool D, bool O, int K, int VPT, int STAGES, bool G>
 cudaError_t launch_stream(const Params& p, int64_t T, bool pdl, cudaStream_t stream,
-                          int device) {
+                          int device, int kc) {
   using C = attn_res_dev::StreamCfg<S, D, O, K, VPT, STAGES>;
   void (*kern)(Params, int64_t) = attn_res_dev::attn_res_stream_kernel<S, D, O, K, VPT, STAGES, G>;
-  // per device: attributes set and the number of co-resident clusters
-  static std::atomic<int> clusters_per_device[64];
-  if (device < 0 || device >= 64) return cudaErrorInvalidDevice;
-  int ncl_max = clusters_per_device[device].load(std::memory_order_acquire);
+  // CTAs per token row: K, or (K = 0, any width) kc = H / 1024 from the caller
+  if (K != 0) kc = K;
+  if (device < 0 || device >= 64 || kc < 1 || kc > attn_res_dev::kRtMaxK)
+    return cudaErrorInvalidValue;
+  // per device and split: attributes set and the number of co-resident clusters
+  static std::atomic<int> clusters_per_device[64][attn_res_dev::kRtMaxK + 1];
+  int ncl_max = clusters_per_device[device][kc].load(std::memory_order_acquire);
   if (ncl_max == 0) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    if (C::COMM && K > 8) {
+    if (C::COMM && kc > 8) {
       e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
       if (e != cudaSuccess) return e;
     }
     if (C::COMM) {
       cudaLaunchAttribute a;
       a.id = cudaLaunchAttributeClusterDimension;
-      a.val.clusterDim.x = K;
+      a.val.clusterDim.x = kc;
       a.val.clusterDim.y = 1;
       a.val.clusterDim.z = 1;
       cudaLaunchConfig_t cfg = {};
-      cfg.gridDim = dim3(K * 1024, 1, 1);
+      cfg.gridDim = dim3(kc * 1024, 1, 1);
       cfg.blockDim = dim3(C::THREADS, 1, 1);
       cfg.dynamicSmemBytes = C::SMEM_BYTES;
       cfg.attrs = &a;
@@ -131,17 +139,17 @@ cudaError_t launch_stream(const Params& p, int64_t T, bool pdl, cudaStream_t str
       if (e != cudaSuccess) return e;
       e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
       if (e != cudaSuccess) return e;
-      ncl_max = per_sm * sms / K;
+      ncl_max = per_sm * sms / kc;
     }
     if (ncl_max < 1) return cudaErrorInvalidConfiguration;
-    clusters_per_device[device].store(ncl_max, std::memory_order_release);
+    clusters_per_device[device][kc].store(ncl_max, std::memory_order_release);
   }
   const int64_t ncl = T < ncl_max ? T : ncl_max;
   cudaLaunchAttribute attrs[2];
   unsigned n = 0;
   if (C::COMM) {
     attrs[n].id = cudaLaunchAttributeClusterDimension;
-    attrs[n].val.clusterDim.x = K;
+    attrs[n].val.clusterDim.x = kc;
     attrs[n].val.clusterDim.y = 1;
     attrs[n].val.clusterDim.z = 1;
     ++n;
@@ -152,7 +160,7 @@ cudaError_t launch_stream(const Params& p, int64_t T, bool pdl, cudaStream_t str
     ++n;
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(ncl * K), 1, 1);
+  cfg.gridDim = dim3(static_cast<unsigned>(ncl * kc), 1, 1);
   cfg.blockDim = dim3(C::THREADS, 1, 1);
   cfg.dynamicSmemBytes = C::SMEM_BYTES;
   cfg.stream = stream;

@@ -38,12 +38,18 @@
 
 namespace attn_res_dev {
 
+// K = 0: any width H that is a multiple of kRtCols -- H / kRtCols CTAs per
+// token row (1..kRtMaxK, read at run time from the cluster shape), each
+// owning kRtCols columns; otherwise K CTAs split the 7168 columns.
+constexpr int kRtCols = 1024;
+constexpr int kRtMaxK = 16;
+
 template <int S, bool HAS_DELTA, bool HAS_ONORM, int K, int VPT, int STAGES>
 struct StreamCfg {
-  static constexpr int VPC = kNV / K;  // vectors per CTA per row
+  static constexpr int VPC = K ? kNV / K : kRtCols / kVec;  // vectors per CTA per row
   static constexpr int THREADS = (VPC / VPT + 31) / 32 * 32;
   static constexpr int NW = THREADS / 32;
-  using Tok = TokenCfg<S, HAS_DELTA, HAS_ONORM, K, NW>;
+  using Tok = TokenCfg<S, HAS_DELTA, HAS_ONORM, K ? K : kRtMaxK, NW>;
   static constexpr bool COMM = Tok::COMM;
   static constexpr uint32_t SLICE_BYTES = VPC * 16;  // one row's slice, multiple of 16
   static constexpr uint32_t STAGE_BYTES = S * SLICE_BYTES;
@@ -60,7 +66,7 @@ struct StreamCfg {
   static constexpr int BY_REGS = 65536 / (THREADS * REG_FLOOR);
   static constexpr int MIN_BLOCKS_RAW = BY_SMEM < BY_REGS ? BY_SMEM : BY_REGS;
   static constexpr int MIN_BLOCKS = MIN_BLOCKS_RAW < 1 ? 1 : MIN_BLOCKS_RAW;
-  static_assert(kNV % K == 0, "split must divide the 896 row vectors");
+  static_assert(K == 0 || kNV % K == 0, "split must divide the 896 row vectors");
   static_assert(VPC % VPT == 0, "vectors per thread must divide the slice");
   static_assert(STAGES >= 2 && STAGES <= 4, "ring depth");
 };
@@ -86,9 +92,11 @@ __global__ void __launch_bounds__(StreamCfg<S, HAS_DELTA, HAS_ONORM, K, VPT, STA
   const int tid = threadIdx.x;
   const int lane = tid & 31;
   const int warp = tid >> 5;
-  const uint32_t rank = COMM ? cluster_ctarank() : (blockIdx.x % K);
-  const int64_t cid = blockIdx.x / K;  // cluster (token group) index
-  const int64_t ncl = gridDim.x / K;   // clusters in the grid
+  // CTAs per token row and 1 / H: constants, or from the cluster shape
+  const Split sp{K ? K : (int)cluster_nctarank(), K ? kInvH : p.inv_h};
+  const uint32_t rank = COMM ? cluster_ctarank() : (blockIdx.x % sp.kc);
+  const int64_t cid = blockIdx.x / sp.kc;  // cluster (token group) index
+  const int64_t ncl = gridDim.x / sp.kc;   // clusters in the grid
   const int64_t ntok = (T > cid) ? (T - cid + ncl - 1) / ncl : 0;
   const int64_t slice0 = (int64_t)rank * VPC * kVec;  // first column of this CTA
   const uint32_t ring_addr = smem_addr(ring);
@@ -181,7 +189,7 @@ __global__ void __launch_bounds__(StreamCfg<S, HAS_DELTA, HAS_ONORM, K, VPT, STA
   auto phase_a = [&](int64_t j, uint4 (&cc)[VPT]) {
     const int s = (int)(j % STAGES);
     const int b = (int)(j & 1);
-    if (COMM && tid == 0) mailbox_expect<Tok>(mb, b, HAS_ONORM);
+    if (COMM && tid == 0) mailbox_expect<Tok>(mb, b, HAS_ONORM, sp);
     current_row<HAS_DELTA, VPT>(pre, del, cc);
     if (j + 1 < ntok) load_current(cid + (j + 1) * ncl, pre, del);
     const bool was_failed = failed;
@@ -189,9 +197,9 @@ __global__ void __launch_bounds__(StreamCfg<S, HAS_DELTA, HAS_ONORM, K, VPT, STA
                  kErrStageTimeout);
     if (tid == 0 && !was_failed && !failed) pending &= ~(1u << s);
     const uint4* stage = stage_of(j);
-    token_sums<S, HAS_DELTA, HAS_ONORM, K, NW, VPT>(
+    token_sums<S, HAS_DELTA, HAS_ONORM, (K ? K : kRtMaxK), NW, VPT>(
         [&](int i, int v) { return active[v] ? stage[i * VPC + v * THREADS] : make_uint4(0, 0, 0, 0); },
-        cc, q, mb, b, rank, warp, lane);
+        cc, q, mb, b, rank, warp, lane, sp);
   };
 
   uint4 c_cur[VPT];
@@ -206,14 +214,14 @@ __global__ void __launch_bounds__(StreamCfg<S, HAS_DELTA, HAS_ONORM, K, VPT, STA
 
     // B(j): softmax and mix; each warp releases the stage after its last read
     f32x2 acc[VPT][4];
-    token_mix<S, HAS_DELTA, HAS_ONORM, K, NW, VPT>(
+    token_mix<S, HAS_DELTA, HAS_ONORM, (K ? K : kRtMaxK), NW, VPT>(
         [&](int i, int v) { return active[v] ? stage[i * VPC + v * THREADS] : make_uint4(0, 0, 0, 0); },
         mb, b, bparity, rank, warp, lane, p.eps, failed, p.err,
         [&]() {
           __syncwarp();
           if (lane == 0) mbar_arrive(smem_addr(&empty_bar[s]));
         },
-        c_cur, acc);
+        c_cur, acc, sp);
 
     // refill stage s with the token STAGES ahead once every local warp is
     // done: thread 0 waits and decides for warp 0; each issuing lane orders
@@ -245,8 +253,8 @@ __global__ void __launch_bounds__(StreamCfg<S, HAS_DELTA, HAS_ONORM, K, VPT, STA
                                             (int64_t)p.write_idx * p.blocks_slot
                                       : nullptr;
     uint4 o[VPT];
-    token_finish<S, HAS_DELTA, HAS_ONORM, K, NW, VPT>(mb, b, bparity, lane, p.out_eps, failed,
-                                                       p.err, ow, acc, o);
+    token_finish<S, HAS_DELTA, HAS_ONORM, (K ? K : kRtMaxK), NW, VPT>(
+        mb, b, bparity, lane, p.out_eps, failed, p.err, ow, acc, o, sp);
 #pragma unroll
     for (int v = 0; v < VPT; ++v) {
       if (active[v]) {

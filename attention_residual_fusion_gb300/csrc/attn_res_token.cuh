@@ -52,7 +52,8 @@ struct TokenCfg {
   static constexpr uint32_t SUMS_BYTES = K * NW * NR * 4;  // expected per token
   static constexpr uint32_t SQ_BYTES = K * NW * 4;
   static constexpr bool COMM = (S > 0) || HAS_ONORM;
-  using Box = Mailbox<K, NW, NR>;
+  static constexpr int NWARPS = NW;
+  using Box = Mailbox<K, NW, NR>;  // sized for up to K CTAs
   static_assert(K * NW <= 32, "one lane per mailbox slot");
 };
 
@@ -65,12 +66,21 @@ __device__ __forceinline__ void mailbox_init(Box& mb) {
   }
 }
 
+// The row split: kc CTAs per token row (<= the K the mailboxes are sized
+// for) and 1 / H for the means.  Kernels built for one width pass constants.
+struct Split {
+  int kc;
+  float inv_h;
+};
+
 // Thread 0, once per token before waiting: the one arrival of this phase,
 // with the byte count the peers' stores will complete.
 template <class Cfg>
-__device__ __forceinline__ void mailbox_expect(typename Cfg::Box& mb, int b, bool has_onorm) {
-  if (Cfg::N > 1) mbar_arrive_expect_tx(smem_addr(&mb.bar_sums[b]), Cfg::SUMS_BYTES);
-  if (has_onorm) mbar_arrive_expect_tx(smem_addr(&mb.bar_sq[b]), Cfg::SQ_BYTES);
+__device__ __forceinline__ void mailbox_expect(typename Cfg::Box& mb, int b, bool has_onorm,
+                                               Split sp) {
+  const uint32_t senders = (uint32_t)(sp.kc * Cfg::NWARPS);
+  if (Cfg::N > 1) mbar_arrive_expect_tx(smem_addr(&mb.bar_sums[b]), senders * Cfg::NR * 4u);
+  if (has_onorm) mbar_arrive_expect_tx(smem_addr(&mb.bar_sq[b]), senders * 4u);
 }
 
 // q = rms_w * res_w for the thread's columns, as fp32 pairs.
@@ -107,7 +117,7 @@ template <int S, bool HAS_DELTA, bool HAS_ONORM, int K, int NW, int VPT, class R
 __device__ __forceinline__ void token_sums(Row row, const uint4 (&c)[VPT],
                                            const f32x2 (&q)[VPT][4],
                                            typename TokenCfg<S, HAS_DELTA, HAS_ONORM, K, NW>::Box& mb,
-                                           int b, uint32_t rank, int warp, int lane) {
+                                           int b, uint32_t rank, int warp, int lane, Split sp) {
   using C = TokenCfg<S, HAS_DELTA, HAS_ONORM, K, NW>;
   constexpr int N = C::N;
   constexpr int NR = C::NR;
@@ -145,7 +155,7 @@ __device__ __forceinline__ void token_sums(Row row, const uint4 (&c)[VPT],
     if ((lane & ((1 << C::SHIFT) - 1)) == 0 && idx < (NR < P ? NR : P)) {
       const uint32_t a = smem_addr(&mb.sums[b][src][idx]);
 #pragma unroll
-      for (int r = 0; r < K; ++r) st_async_f32(map_rank(a, r), tv, map_rank(bar, r));
+      for (int r = 0; r < sp.kc; ++r) st_async_f32(map_rank(a, r), tv, map_rank(bar, r));
     }
     if constexpr (C::NR2 > 0) {
       float hi[P2];
@@ -156,7 +166,7 @@ __device__ __forceinline__ void token_sums(Row row, const uint4 (&c)[VPT],
       if ((lane & ((1 << C::SHIFT2) - 1)) == 0 && idx2 < C::NR2) {
         const uint32_t a = smem_addr(&mb.sums[b][src][P + idx2]);
 #pragma unroll
-        for (int r = 0; r < K; ++r) st_async_f32(map_rank(a, r), tv2, map_rank(bar, r));
+        for (int r = 0; r < sp.kc; ++r) st_async_f32(map_rank(a, r), tv2, map_rank(bar, r));
       }
     }
   }
@@ -170,7 +180,7 @@ __device__ __forceinline__ void token_mix(Row row,
                                           int b, uint32_t parity, uint32_t rank, int warp,
                                           int lane, float eps, bool& failed, unsigned* err,
                                           AfterMix after_mix, const uint4 (&c)[VPT],
-                                          f32x2 (&acc)[VPT][4]) {
+                                          f32x2 (&acc)[VPT][4], Split sp) {
   using C = TokenCfg<S, HAS_DELTA, HAS_ONORM, K, NW>;
   constexpr int N = C::N;
   constexpr int NR = C::NR;
@@ -186,14 +196,14 @@ __device__ __forceinline__ void token_mix(Row row,
     float tot = 0.f;
     if (lane < NR) {
 #pragma unroll 4
-      for (int s = 0; s < K * NW; ++s) tot += mb.sums[b][s][lane];
+      for (int s = 0; s < sp.kc * NW; ++s) tot += mb.sums[b][s][lane];
     }
     const float dtv = __shfl_sync(0xffffffffu, tot, (lane + N) & 31);
     float logit = __int_as_float(0xff800000u);  // -inf
     // reciprocal square root and a fast quotient (z in [1, N]): a few ulp of
     // fp32 on the weights, far below the bf16 output's resolution, and the
     // same instructions in every warp, so the weights stay bit-identical
-    if (lane < N) logit = dtv * rsqrtf(fmaf(tot, kInvH, eps));
+    if (lane < N) logit = dtv * rsqrtf(fmaf(tot, sp.inv_h, eps));
     const float m = warp_max(logit);
     const float e = (lane < N) ? expf(logit - m) : 0.f;
     const float z = warp_sum(e);
@@ -222,7 +232,7 @@ __device__ __forceinline__ void token_mix(Row row,
 #pragma unroll
       for (int k = 0; k < 4; ++k) sq2 = f2_fma(acc[v][k], acc[v][k], sq2);
     const float sq = warp_sum(f2_lo(sq2) + f2_hi(sq2));
-    if (lane < K)
+    if (lane < sp.kc)
       st_async_f32(map_rank(smem_addr(&mb.sq[b][(int)rank * NW + warp]), lane), sq,
                    map_rank(smem_addr(&mb.bar_sq[b]), lane));
   }
@@ -232,11 +242,11 @@ template <int S, bool HAS_DELTA, bool HAS_ONORM, int K, int NW, int VPT>
 __device__ __forceinline__ void token_finish(typename TokenCfg<S, HAS_DELTA, HAS_ONORM, K, NW>::Box& mb,
                                              int b, uint32_t parity, int lane, float out_eps,
                                              bool& failed, unsigned* err, const uint4 (&ow)[VPT],
-                                             f32x2 (&acc)[VPT][4], uint4 (&out)[VPT]) {
+                                             f32x2 (&acc)[VPT][4], uint4 (&out)[VPT], Split sp) {
   if constexpr (HAS_ONORM) {
     wait_or_flag(smem_addr(&mb.bar_sq[b]), parity, failed, err, kErrExchangeTimeout);
-    const float tot = warp_sum(lane < K * NW ? mb.sq[b][lane] : 0.f);
-    const float ro = rsqrtf(fmaf(tot, kInvH, out_eps));
+    const float tot = warp_sum(lane < sp.kc * NW ? mb.sq[b][lane] : 0.f);
+    const float ro = rsqrtf(fmaf(tot, sp.inv_h, out_eps));
     const f32x2 ro2 = f2_make(ro, ro);
 #pragma unroll
     for (int v = 0; v < VPT; ++v)
@@ -261,13 +271,13 @@ __device__ __forceinline__ void mix_token(Row row, const f32x2 (&q)[VPT][4],
                                           int b, uint32_t parity, uint32_t rank, int warp,
                                           int lane, float eps, float out_eps, bool& failed,
                                           unsigned* err, AfterMix after_mix, const uint4 (&c)[VPT],
-                                          uint4 (&out)[VPT]) {
+                                          uint4 (&out)[VPT], Split sp) {
   f32x2 acc[VPT][4];
-  token_sums<S, HAS_DELTA, HAS_ONORM, K, NW, VPT>(row, c, q, mb, b, rank, warp, lane);
+  token_sums<S, HAS_DELTA, HAS_ONORM, K, NW, VPT>(row, c, q, mb, b, rank, warp, lane, sp);
   token_mix<S, HAS_DELTA, HAS_ONORM, K, NW, VPT>(row, mb, b, parity, rank, warp, lane, eps, failed,
-                                                 err, after_mix, c, acc);
+                                                 err, after_mix, c, acc, sp);
   token_finish<S, HAS_DELTA, HAS_ONORM, K, NW, VPT>(mb, b, parity, lane, out_eps, failed, err, ow,
-                                                    acc, out);
+                                                    acc, out, sp);
 }
 
 }  // namespace attn_res_dev

@@ -210,7 +210,34 @@ def test_other_widths_validate_strides(lib):
     assert ar.call_raw(**kw, H=64) == 1             # stride below H
     kw = good_h(64)
     kw["layout"].flags = ar.FLAG_KERNEL(2)
-    assert ar.call_raw(**kw, H=64) == 1             # only the general kernel takes other widths
+    assert ar.call_raw(**kw, H=64) == 1             # the stream kernel wants H a multiple of 1024
+    kw["layout"].flags = ar.FLAG_KERNEL(1)
+    assert ar.call_raw(**kw, H=64) == 1             # the split kernel is built for 7168 only
+
+
+def test_any_width_stream_checks(lib):
+    """Multiples of 1024 up to 16384 may take the stream kernel's any-width
+    form, in its one shape; other widths and shape overrides may not."""
+    import torch
+    no_gpu = not torch.cuda.is_available()
+    for Hh in (1024, 4096, 16384):
+        kw = good_h(Hh, T=200)
+        kw["layout"].flags = ar.FLAG_KERNEL(2)
+        if no_gpu:
+            assert ar.call_raw(**kw, H=Hh) in (4, 5)
+        kw["layout"].flags = ar.FLAG_KERNEL(2) | ar.FLAG_VPT(2)
+        assert ar.call_raw(**kw, H=Hh) == 1
+    for Hh in (17408, 4000, 1536):                   # 17 CTAs; not a multiple of 1024
+        kw = good_h(Hh, T=200)
+        kw["layout"].flags = ar.FLAG_KERNEL(2)
+        assert ar.call_raw(**kw, H=Hh) == 1
+        kw["layout"].flags = 0                      # automatic: the general kernel
+        if no_gpu:
+            assert ar.call_raw(**kw, H=Hh) in (4, 5)
+    kw = good_h(4096, T=200, S=0)
+    kw["out_norm_w"] = 0
+    kw["layout"].flags = ar.FLAG_KERNEL(2)           # no exchange: not a stream case
+    assert ar.call_raw(**kw, H=4096) == 1
 
 
 # ---- hidden-sharded entry points (host checks only) ----

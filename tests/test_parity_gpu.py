@@ -356,3 +356,33 @@ def test_nonfinite_inputs_stay_in_their_token(kernel):
         assert np.all(np.isnan(R.widen(gpu["out"][t]))), t
     assert _nan_equal(gpu["prefix"], ref["prefix"][:, :wl.H])
     assert _nan_equal(gpu["bank"], ref["bank"])
+
+
+
+# ---- other widths on the stream kernel (H a multiple of 1024) ---------------------
+
+ANYW = [(H, S) for H in (1024, 2048, 3072, 4096, 8192, 16384) for S in (0, 4, 8)]
+
+
+@pytest.mark.parametrize("H,S", ANYW, ids=[f"H{H}_S{S}" for H, S in ANYW])
+def test_any_width_stream(H, S):
+    """H / 1024 CTAs per token row; ragged token count over the clusters,
+    padded bank slots, delta / write-back varying by case; automatic choice
+    (T >= 80 with bank rows or an output norm streams)."""
+    i = H // 1024 + S
+    wl = W.make_workload(131, S, capacity=9, has_delta=bool(i & 1), has_out_norm=True,
+                         block_write_idx=[-1, S, 8][i % 3],
+                         seed=900 + i, H=H, mixing=True, slot_stride=H + 8 * (i % 2))
+    full_check(wl, tag=f"anywidth_H{H}_S{S}")
+
+
+@pytest.mark.parametrize("H", [2048, 12288])
+def test_any_width_stream_forced_small_T_and_groups(H):
+    """Forced at few tokens (more clusters than tokens), no output norm, and
+    with shared bank rows (B = 3)."""
+    wl = W.make_workload(5, 8, capacity=9, has_delta=True, has_out_norm=False,
+                         block_write_idx=8, seed=H, H=H, mixing=True)
+    full_check(wl, tag=f"anywidth_forced_H{H}", kernel=ar.KERNEL_STREAM)
+    wl = W.make_workload(200, 6, capacity=8, has_delta=True, has_out_norm=True,
+                         block_write_idx=7, seed=H + 1, H=H, mixing=True, group=3)
+    full_check(wl, tag=f"anywidth_group_H{H}")
