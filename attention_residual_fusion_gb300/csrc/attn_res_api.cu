@@ -371,8 +371,9 @@ attn_res_status_t run(int64_t H, attn_res_bf16_t* prefix, const attn_res_bf16_t*
                 &plan) != ATTN_RES_OK)
     return ATTN_RES_EINVAL;
   // other widths: the stream kernel's any-width form when H is a multiple
-  // of 1024 (at most 16 CTAs per row) and the call would stream, else the
-  // general kernel; no shape overrides
+  // of 1024 (at most 16 CTAs per row) and the CTAs of a row exchange sums
+  // (at any T: at few tokens it is within ~10 % of the split kernel), else
+  // the general kernel; no shape overrides
   if (H != kH) {
     const uint32_t f = layout->flags;
     const int forced = static_cast<int>((f >> 16) & 0xfu);
@@ -384,8 +385,7 @@ attn_res_status_t run(int64_t H, attn_res_bf16_t* prefix, const attn_res_bf16_t*
     if (forced == ATTN_RES_KERNEL_STREAM && (!any_width || overrides || !exchange))
       return ATTN_RES_EINVAL;
     const bool stream_it = forced == ATTN_RES_KERNEL_STREAM ||
-                           (forced == 0 && !overrides && any_width && exchange &&
-                            T >= kStreamMinTokens);
+                           (forced == 0 && !overrides && any_width && exchange);
     if (stream_it) {
       plan.kernel = ATTN_RES_KERNEL_STREAM;
       plan.shape = kAnyWidthStreamShape;

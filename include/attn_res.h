@@ -170,11 +170,10 @@ attn_res_status_t attn_res(attn_res_bf16_t* prefix, const attn_res_bf16_t* delta
  * multiple of 8 (one 16-byte vector); every [H]- and row-sized argument above
  * is then H elements wide and strides must be >= H.  H == ATTN_RES_HIDDEN
  * behaves exactly like attn_res.  Other widths:
- *   - H a multiple of 1024, at most 16384, from 80 token rows (with bank rows
- *     or an output norm): the stream kernel in an any-width form, H / 1024
- *     CTAs per token row (one cluster), each with the per-CTA layout of the
- *     (7,2,2) shape; ATTN_RES_FLAG_KERNEL(ATTN_RES_KERNEL_STREAM) forces it at
- *     any T; other shape overrides are ATTN_RES_EINVAL;
+ *   - H a multiple of 1024, at most 16384, with bank rows or an output norm:
+ *     the stream kernel in an any-width form, H / 1024 CTAs per token row
+ *     (one cluster), each with the per-CTA layout of the (7,2,2) shape;
+ *     shape overrides are ATTN_RES_EINVAL;
  *   - otherwise a general kernel (one CTA of 256 threads per token row, same
  *     fp32 arithmetic, the rows read three times through L2), a functional
  *     path.  ATTN_RES_FLAG_KERNEL(ATTN_RES_KERNEL_GENERIC) forces it, also at
