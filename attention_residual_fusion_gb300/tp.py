@@ -110,16 +110,26 @@ CUDA_PHASES = types.SimpleNamespace(sums=tp_sums, sq=tp_sq, finish=tp_finish)
 def attn_res_tp(prefix, delta, blocks, num_blocks: int, block_write_idx: int, res_w, rms_w,
                 out_norm_w=None, eps: float = 1e-6, out_eps: float = 1e-6, out=None, *,
                 H: int | None = None, group=None, all_reduce=None, phases=None,
-                gram: bool = False, pdl: bool = False, blocks_group: int = 1, stream=None):
+                gram: bool = False, pdl: bool = False, blocks_group: int = 1,
+                chunk_tokens: int | None = None, stream=None):
     """The mixture on this rank's column shard (every row-sized argument is
     the shard, width ``res_w.shape[0]``).  ``H`` is the full width (default:
     shard width x world size of ``group``).  ``all_reduce(tensor)`` sums a
-    float32 tensor in place over the ranks (default torch.distributed's
-    all_reduce on ``group``; with no process group initialised the call is
-    local).  ``gram`` selects the single-exchange form; ``blocks_group`` as
-    for attn_res.  With ``stream`` given, the buffers, the kernels and the
-    all-reduces are all ordered on that stream.  Returns ``out`` (allocated
-    if not given)."""
+    float32 tensor in place over the ranks and may return a handle with
+    ``wait()`` (default: torch.distributed's asynchronous all_reduce on
+    ``group``; with no process group initialised the call is local).
+    ``gram`` selects the single-exchange form; ``blocks_group`` as for
+    attn_res.
+
+    ``chunk_tokens`` runs the token rows in chunks, software-pipelined: the
+    first kernel of chunk c+1 is issued while the all-reduce of chunk c is in
+    flight, and a chunk's later passes follow its first closely enough to
+    find its rows in L2 (a chunk of 1024 rows of an 896-column shard with 8
+    bank rows is 18 MB).  It must be a multiple of ``blocks_group``.  Every
+    rank must pass the same value: the all-reduces are matched by order.
+
+    With ``stream`` given, the buffers, the kernels and the all-reduces are
+    all ordered on that stream.  Returns ``out`` (allocated if not given)."""
     import contextlib
 
     import torch
@@ -128,11 +138,17 @@ def attn_res_tp(prefix, delta, blocks, num_blocks: int, block_write_idx: int, re
     with ctx:
         return _attn_res_tp(prefix, delta, blocks, num_blocks, block_write_idx, res_w, rms_w,
                             out_norm_w, eps, out_eps, out, H, group, all_reduce, phases, gram,
-                            pdl, blocks_group, stream)
+                            pdl, blocks_group, chunk_tokens, stream)
+
+
+def _wait(handle) -> None:
+    if handle is not None and hasattr(handle, "wait"):
+        handle.wait()
 
 
 def _attn_res_tp(prefix, delta, blocks, num_blocks, block_write_idx, res_w, rms_w, out_norm_w,
-                 eps, out_eps, out, H, group, all_reduce, phases, gram, pdl, blocks_group, stream):
+                 eps, out_eps, out, H, group, all_reduce, phases, gram, pdl, blocks_group,
+                 chunk_tokens, stream):
     import torch
     import torch.distributed as dist
 
@@ -144,26 +160,69 @@ def _attn_res_tp(prefix, delta, blocks, num_blocks, block_write_idx, res_w, rms_
     if all_reduce is None:
         if dist_on:
             def all_reduce(t):
-                dist.all_reduce(t, op=dist.ReduceOp.SUM, group=group)
+                return dist.all_reduce(t, op=dist.ReduceOp.SUM, group=group, async_op=True)
         else:
             def all_reduce(t):
                 return None
+    B = max(1, int(blocks_group))
+    if chunk_tokens is None or chunk_tokens <= 0 or chunk_tokens >= T:
+        chunk = max(T, 1)
+    else:
+        chunk = int(chunk_tokens)
+        if chunk % B:
+            raise ValueError("chunk_tokens must be a multiple of blocks_group")
     ph = phases or CUDA_PHASES
     dev = prefix.device
     if out is None:
         out = torch.empty((T, Hs), dtype=prefix.dtype, device=dev)
     gram = bool(gram and out_norm_w is not None)  # the Gram entries serve the output norm only
+    two = out_norm_w is not None and not gram     # second exchange (sum of squares)
     sums = torch.empty((T, sums_width(num_blocks, gram)), dtype=torch.float32, device=dev)
+    sq = torch.empty((T,), dtype=torch.float32, device=dev) if two else None
     kw = dict(pdl=pdl, stream=stream)
-    if blocks_group != 1:
-        kw["blocks_group"] = blocks_group
-    ph.sums(prefix, delta, blocks, num_blocks, res_w, rms_w, sums, gram=gram, **kw)
-    all_reduce(sums)
-    sq = None
-    if out_norm_w is not None and not gram:
-        sq = torch.empty((T,), dtype=torch.float32, device=dev)
-        ph.sq(prefix, delta, blocks, num_blocks, H, eps, sums, sq, **kw)
-        all_reduce(sq)
-    ph.finish(prefix, delta, blocks, num_blocks, block_write_idx, H, out_norm_w, eps, out_eps,
-              sums, sq, out, gram=gram, **kw)
+    if B != 1:
+        kw["blocks_group"] = B
+
+    bounds = [(c0, min(T, c0 + chunk)) for c0 in range(0, T, chunk)] or [(0, 0)]
+
+    def rows(c):
+        c0, c1 = bounds[c]
+        bank = None if blocks is None else blocks[c0 // B:-(-c1 // B)]
+        return (prefix[c0:c1], None if delta is None else delta[c0:c1], bank,
+                out[c0:c1], sums[c0:c1], None if sq is None else sq[c0:c1])
+
+    def first(c):
+        p_, d_, b_, _, s_, _ = rows(c)
+        ph.sums(p_, d_, b_, num_blocks, res_w, rms_w, s_, gram=gram, **kw)
+        return all_reduce(s_)
+
+    def second(c):
+        p_, d_, b_, _, s_, q_ = rows(c)
+        ph.sq(p_, d_, b_, num_blocks, H, eps, s_, q_, **kw)
+        return all_reduce(q_)
+
+    def last(c):
+        p_, d_, b_, o_, s_, q_ = rows(c)
+        ph.finish(p_, d_, b_, num_blocks, block_write_idx, H, out_norm_w, eps, out_eps, s_, q_,
+                  o_, gram=gram, **kw)
+
+    # software pipeline over the chunks: chunk c+1's first pass overlaps the
+    # exchange of chunk c, and the finish of chunk c-1 that of chunk c
+    n = len(bounds)
+    h1 = {0: first(0)}
+    h2 = {}
+    for c in range(n):
+        if c + 1 < n:
+            h1[c + 1] = first(c + 1)
+        _wait(h1.pop(c))
+        if two:
+            h2[c] = second(c)
+            if c > 0:
+                _wait(h2.pop(c - 1))
+                last(c - 1)
+        else:
+            last(c)
+    if two:
+        _wait(h2.pop(n - 1))
+        last(n - 1)
     return out

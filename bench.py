@@ -379,12 +379,12 @@ def tp_cells(ar, torch, dev, stream, peak, ranks=8):
         n = min(16, max(1, -(-3 * l2 // alg)))
         sets = [shard] + [{k: (v.clone() if v is not None and k in ("prefix", "delta", "bank", "out")
                                else v) for k, v in shard.items()} for _ in range(n - 1)]
-        for gram in (False, True):
+        for gram, chunk in ((False, None), (True, None)):
             def step(st):
                 tp.attn_res_tp(st["prefix"], st["delta"], st["bank"], wl.num_blocks,
                                wl.block_write_idx, st["res"], st["rms"], st["onw"], wl.eps,
                                wl.out_eps, st["out"], H=wl.H, all_reduce=lambda x: None,
-                               gram=gram, stream=stream)
+                               gram=gram, chunk_tokens=chunk, stream=stream)
             calls = 16 if wl.T > 1 else 64
             with torch.cuda.stream(stream):
                 for st in sets:
@@ -406,9 +406,13 @@ def tp_cells(ar, torch, dev, stream, peak, ranks=8):
             del g
             us = a.elapsed_time(b) * 1e3 / calls
             gbs = alg / (us * 1e-6) / 1e9
-            rows.append({"workload": f"{name} shard 1/{ranks} (H_s={Hs})",
-                         "form": "single exchange (Gram)" if gram else "two exchanges",
-                         "kernels": 2 if gram else 3, "all_reduces": 1 if gram else 2,
+            nch = -(-wl.T // chunk) if chunk else 1
+            form = "single exchange (Gram)" if gram else "two exchanges"
+            if chunk:
+                form += f", pipelined chunks of {chunk} rows"
+            rows.append({"workload": f"{name} shard 1/{ranks} (H_s={Hs})", "form": form,
+                         "kernels": (2 if gram else 3) * nch,
+                         "all_reduces": (1 if gram else 2) * nch,
                          "us_per_step": round(us, 3), "tokens_per_s": round(wl.T / (us * 1e-6), 1),
                          "gbs": round(gbs, 1), "frac": round(gbs / peak, 4),
                          "input_sets": len(sets)})

@@ -125,6 +125,10 @@ def _tensor(bits):
     return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16)
 
 
+def _chunk(case):
+    return case[6] if len(case) > 6 else None
+
+
 def _rank(rank, world, port, cases, out):
     import torch.distributed as dist
     from attention_residual_fusion_gb300 import tp
@@ -143,7 +147,7 @@ def _rank(rank, world, port, cases, out):
             res = tp.attn_res_tp(prefix, delta, bank, wl.num_blocks, wl.block_write_idx,
                                  _tensor(wl.res_w[a:b]), _tensor(wl.rms_w[a:b]), onw,
                                  wl.eps, wl.out_eps, phases=STANDIN,
-                                 gram=len(case) > 5 and case[5])
+                                 gram=len(case) > 5 and case[5], chunk_tokens=_chunk(case))
             out[(k, rank)] = (_bits(res), _bits(prefix), _bits(bank))
     finally:
         dist.destroy_process_group()
@@ -151,7 +155,8 @@ def _rank(rank, world, port, cases, out):
 
 CASES = [(8, True, True, 8, 256), (4, False, True, 2, 128), (0, True, False, 0, 64),
          (1, False, False, -1, 64), (8, True, False, 3, 512), (8, True, True, 8, 256, True),
-         (2, False, True, -1, 64, True)]
+         (2, False, True, -1, 64, True), (8, True, True, 8, 256, False, 4),
+         (4, True, True, 4, 128, True, 2), (3, False, False, 3, 64, False, 5)]
 
 
 def test_two_gloo_ranks_compose_to_the_oracle():
@@ -210,6 +215,22 @@ def test_reductions_are_called_in_order():
                    _tensor(wl.res_w), _tensor(wl.rms_w), _tensor(wl.out_norm_w), H=64,
                    all_reduce=fake_reduce, phases=STANDIN, gram=True)
     assert seen == [(6, 54)]
+    # chunks of 2 rows: chunk c+1's sums are reduced before chunk c's sum of
+    # squares, and a finish waits for its own chunk's reduction only
+    seen.clear()
+    tp.attn_res_tp(_tensor(wl.prefix.copy()), _tensor(wl.delta), _tensor(wl.bank.copy()), 8, 8,
+                   _tensor(wl.res_w), _tensor(wl.rms_w), _tensor(wl.out_norm_w), H=64,
+                   all_reduce=fake_reduce, phases=STANDIN, chunk_tokens=2)
+    assert seen == [(2, 18), (2, 18), (2,), (2, 18), (2,), (2,)]
+    seen.clear()
+    tp.attn_res_tp(_tensor(wl.prefix.copy()), _tensor(wl.delta), _tensor(wl.bank.copy()), 8, 8,
+                   _tensor(wl.res_w), _tensor(wl.rms_w), _tensor(wl.out_norm_w), H=64,
+                   all_reduce=fake_reduce, phases=STANDIN, chunk_tokens=4, gram=True)
+    assert seen == [(4, 54), (2, 54)]
+    with pytest.raises(ValueError):
+        tp.attn_res_tp(_tensor(wl.prefix.copy()), _tensor(wl.delta), _tensor(wl.bank.copy()), 8,
+                       8, _tensor(wl.res_w), _tensor(wl.rms_w), _tensor(wl.out_norm_w), H=64,
+                       all_reduce=fake_reduce, phases=STANDIN, chunk_tokens=3, blocks_group=2)
 
 
 def test_standins_pin_to_the_oracle_unsharded():

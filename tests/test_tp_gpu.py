@@ -56,7 +56,7 @@ class ThreadGroup:
         return fn
 
 
-def run_tp_ranks(wl: W.Workload, widths, *, pdl=False, out_row=None, gram=False):
+def run_tp_ranks(wl: W.Workload, widths, *, pdl=False, out_row=None, gram=False, chunk=None):
     """Run attn_res_tp on every column shard (one thread per rank) over guarded
     device copies of the workload; return host copies like gpu_util.run_gpu."""
     import torch
@@ -86,7 +86,7 @@ def run_tp_ranks(wl: W.Workload, widths, *, pdl=False, out_row=None, gram=False)
                     g_res.view[a:b], g_rms.view[a:b],
                     None if g_onw is None else g_onw.view[a:b], wl.eps, wl.out_eps,
                     g_out.view[:, a:b], H=H, all_reduce=group.all_reduce_for(r), gram=gram,
-                    pdl=pdl, blocks_group=wl.group, stream=stream)
+                    pdl=pdl, blocks_group=wl.group, chunk_tokens=chunk, stream=stream)
         except BaseException as e:  # noqa: BLE001 - reported below
             errors.append(e)
             group.barrier.abort()
@@ -99,7 +99,8 @@ def run_tp_ranks(wl: W.Workload, widths, *, pdl=False, out_row=None, gram=False)
     if errors:
         raise errors[0]
     torch.cuda.synchronize()
-    expect_calls = 2 if (wl.out_norm_w is not None and not gram) else 1
+    chunks = -(-wl.T // chunk) if chunk else 1
+    expect_calls = (2 if (wl.out_norm_w is not None and not gram) else 1) * max(chunks, 1)
     assert group.calls == [expect_calls] * len(widths)
     bufs = [g for g in (g_prefix, g_delta, g_bank, g_rms, g_res, g_onw, g_out) if g is not None]
     assert all(g.guards_intact() for g in bufs), "a guard zone was written"
@@ -218,3 +219,11 @@ def test_shared_bank_rows(B, widx, gram):
     wl = W.make_workload(23, 8, capacity=9, has_delta=True, has_out_norm=True,
                          block_write_idx=widx, seed=60 + B, mixing=True, group=B)
     tp_check(wl, [W.HIDDEN // 4] * 4, f"tp_group{B}", gram=gram)
+
+
+@pytest.mark.parametrize("gram,chunk,B", [(False, 16, 1), (True, 16, 1), (False, 12, 3), (True, 7, 1)])
+def test_chunked_pipeline(gram, chunk, B):
+    """Token chunks, software-pipelined (ragged last chunk), over four shards."""
+    wl = W.make_workload(61, 8, capacity=9, has_delta=True, has_out_norm=True,
+                         block_write_idx=8, seed=80 + chunk, mixing=True, group=B)
+    tp_check(wl, [W.HIDDEN // 4] * 4, f"tp_chunk{chunk}", gram=gram, chunk=chunk)
