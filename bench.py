@@ -11,7 +11,8 @@ than L2, so no flush is needed between steps.
              inputs resident in HBM, max over ranks, summed over ranks
   e2e        the same metric through the public call with pinned HOST
              buffers: every step copies its inputs host->device and reads
-             out, the updated prefix and the written bank slot back
+             out, the updated prefix and the written bank slot back; steps
+             pipelined over copy-in / compute / copy-out streams
   roofline   algorithmic bytes per launch / mean launch time vs the measured
              HBM copy bandwidth
   latency_us T=1 latency (single-token and 8-block cases): per call with an
@@ -508,13 +509,17 @@ def latency_t1(ar, torch, dev, stream, reps=200):
 
 
 def e2e(ar, wl, torch, dev, stream, steps):
-    """Through the public call with pinned host buffers: H2D of every input,
-    the call, D2H of out, the updated prefix and the written bank slot."""
+    """Through the public call with pinned host buffers: every step copies all
+    of its inputs host->device, makes the call and reads out, the updated
+    prefix and the written bank slot back.  Steps are pipelined over a
+    copy-in stream, the compute stream and a copy-out stream with two device
+    input sets, so step k+1's inputs go up while step k's results come down
+    (the host link carries both directions at once)."""
     pin = lambda a: torch.from_numpy(a.view(np.int16)).pin_memory().view(torch.bfloat16)
     hp = dict(prefix=pin(wl.prefix), delta=None if wl.delta is None else pin(wl.delta),
               bank=pin(wl.bank), rms=pin(wl.rms_w), res=pin(wl.res_w),
               onw=None if wl.out_norm_w is None else pin(wl.out_norm_w))
-    d = device_tensors(wl, torch, dev)
+    sets = [device_tensors(wl, torch, dev) for _ in range(2)]
     h_out = torch.empty((wl.T, wl.H), dtype=torch.bfloat16).pin_memory()
     h_pre = torch.empty((wl.T, wl.H), dtype=torch.bfloat16).pin_memory()
     h_slot = torch.empty((wl.T, wl.H), dtype=torch.bfloat16).pin_memory() \
@@ -522,38 +527,53 @@ def e2e(ar, wl, torch, dev, stream, steps):
     h2d = sum(v.numel() * 2 for v in hp.values() if v is not None)
     d2h = h_out.numel() * 2 + (h_pre.numel() * 2 if wl.delta is not None else 0) + \
         (h_slot.numel() * 2 if h_slot is not None else 0)
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_call = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
+    for e in ev_in + ev_call + ev_out:
+        e.record(stream)
 
-    def step():
-        with torch.cuda.stream(stream):
-            for k, v in hp.items():
+    def step(k):
+        i = k % 2
+        d = sets[i]
+        s_in.wait_event(ev_out[i])        # set i is free once step k-2 is read back
+        with torch.cuda.stream(s_in):
+            for key, v in hp.items():
                 if v is not None:
-                    d[k].copy_(v, non_blocking=True)
-            call(ar, wl, d, stream)
+                    d[key].copy_(v, non_blocking=True)
+            ev_in[i].record(s_in)
+        stream.wait_event(ev_in[i])
+        call(ar, wl, d, stream)
+        ev_call[i].record(stream)
+        s_out.wait_event(ev_call[i])
+        with torch.cuda.stream(s_out):
             h_out.copy_(d["out"], non_blocking=True)
             if wl.delta is not None:
                 h_pre.copy_(d["prefix"], non_blocking=True)
             if h_slot is not None:
                 h_slot.copy_(d["bank"][:, wl.block_write_idx, : wl.H], non_blocking=True)
+            ev_out[i].record(s_out)
 
-    step()
+    step(0)
+    step(1)
     torch.cuda.synchronize()
     a = torch.cuda.Event(enable_timing=True)
     b = torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        a.record(stream)
+    a.record(s_in)
     w0 = time.perf_counter()
-    for _ in range(steps):
-        step()
-    with torch.cuda.stream(stream):
-        b.record(stream)
+    for k in range(steps):
+        step(k)
+    b.record(s_out)
     torch.cuda.synchronize()
     wall = time.perf_counter() - w0
     ms = a.elapsed_time(b)
-    del d, hp
+    del sets, hp
     return {"value": wl.T * steps / (ms / 1e3), "unit": "tokens/s",
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
             "steps": steps, "ms_per_step": ms / steps,
-            "host_wall_ms_per_step": wall * 1e3 / steps}
+            "host_wall_ms_per_step": wall * 1e3 / steps,
+            "pipeline": "copy-in / compute / copy-out streams, two device input sets"}
 
 
 def run_ours(args, rank, world, local_rank, dist):
