@@ -129,7 +129,8 @@ typedef struct {
  *   prefix          [T, H] at prefix_row.  Read; overwritten with c when
  *                   delta != NULL.
  *   delta           [T, H] at delta_row, or NULL.
- *   blocks          bank [T, capacity, H] at (blocks_token, blocks_slot).
+ *   blocks          bank [T, capacity, H] at (blocks_token, blocks_slot)
+ *                   ([ceil(T / B), capacity, H] with shared bank rows).
  *                   Slots 0 .. num_blocks-1 are read; slot block_write_idx
  *                   (if >= 0) is overwritten with c; nothing else is touched.
  *                   May be NULL only when num_blocks == 0 and
