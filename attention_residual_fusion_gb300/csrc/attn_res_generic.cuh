@@ -10,8 +10,9 @@
 //   3. acc = sum_i w_i x_i, output (normalised when asked), and the
 //      write-backs of c -- each thread writes only vectors it alone reads, so
 //      no barrier is needed between its reads and its writes.
-// This is the functional path for other model widths and for checking the
-// GPU arithmetic at tiny H; H = 7168 uses the split and stream kernels.
+// This is the functional path for widths that are not multiples of 1024 and
+// for checking the GPU arithmetic at tiny H; H = 7168 uses the split and
+// stream kernels, other multiples of 1024 the stream kernel's any-width form.
 #pragma once
 
 #include "attn_res_common.cuh"
