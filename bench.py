@@ -576,6 +576,15 @@ def e2e(ar, wl, torch, dev, stream, steps):
             "pipeline": "copy-in / compute / copy-out streams, two device input sets"}
 
 
+def device_info(torch, dev) -> dict:
+    """Device metadata for the JSON line."""
+    pr = torch.cuda.get_device_properties(dev)
+    return {"name": pr.name, "cc": f"{pr.major}.{pr.minor}", "sms": pr.multi_processor_count,
+            "l2_bytes": getattr(pr, "L2_cache_size", None),
+            "hbm_bytes": pr.total_memory, "torch": torch.__version__,
+            "cuda_runtime": torch.version.cuda}
+
+
 def run_ours(args, rank, world, local_rank, dist):
     import torch
     import attention_residual_fusion_gb300 as ar
@@ -636,6 +645,7 @@ def run_ours(args, rank, world, local_rank, dist):
                      "kernel": kernel_label(wl, shape)},
         "gpu_launches": args.steps,
         "clocks": clk.summary(),
+        "device": device_info(torch, dev),
     }
     if rank == 0 and not args.no_latency:
         line["latency_us"] = latency_t1(ar, torch, dev, stream)
