@@ -370,10 +370,10 @@ attn_res_status_t run(int64_t H, attn_res_bf16_t* prefix, const attn_res_bf16_t*
   if (make_plan(T, num_blocks, out_norm_w != nullptr, layout->flags, bank_group(layout) > 1,
                 &plan) != ATTN_RES_OK)
     return ATTN_RES_EINVAL;
-  // other widths: the stream kernel's any-width form when H is a multiple
-  // of 1024 (at most 16 CTAs per row) and the CTAs of a row exchange sums
-  // (at any T: at few tokens it is within ~10 % of the split kernel), else
-  // the general kernel; no shape overrides
+  // other widths, when H is a multiple of 1024 and the CTAs of a row
+  // exchange sums: the any-width forms -- the split kernel below 80 tokens
+  // (up to 8 CTAs per row), else the stream kernel (up to 16); otherwise the
+  // general kernel; no shape overrides
   if (H != kH) {
     const uint32_t f = layout->flags;
     const int forced = static_cast<int>((f >> 16) & 0xfu);
@@ -381,15 +381,20 @@ attn_res_status_t run(int64_t H, attn_res_bf16_t* prefix, const attn_res_bf16_t*
     const bool any_width = H % attn_res_dev::kRtCols == 0 &&
                            H / attn_res_dev::kRtCols <= attn_res_dev::kRtMaxK;
     const bool exchange = num_blocks > 0 || out_norm_w != nullptr;
-    if (forced == ATTN_RES_KERNEL_SPLIT) return ATTN_RES_EINVAL;
     if (forced == ATTN_RES_KERNEL_STREAM && (!any_width || overrides || !exchange))
       return ATTN_RES_EINVAL;
-    const bool stream_it = forced == ATTN_RES_KERNEL_STREAM ||
-                           (forced == 0 && !overrides && any_width && exchange);
-    if (stream_it) {
+    const int kc = static_cast<int>(H / attn_res_dev::kRtCols);
+    const bool split_ok = any_width && exchange && kc <= attn_res_dev::kSplitRtMaxK;
+    if (forced == ATTN_RES_KERNEL_SPLIT && (!split_ok || overrides)) return ATTN_RES_EINVAL;
+    const bool auto_fast = forced == 0 && !overrides && any_width && exchange;
+    if (forced == ATTN_RES_KERNEL_SPLIT ||
+        (auto_fast && split_ok && T < kStreamMinTokens)) {
+      plan.kernel = ATTN_RES_KERNEL_SPLIT;
+      plan.split = kc;
+    } else if (forced == ATTN_RES_KERNEL_STREAM || auto_fast) {
       plan.kernel = ATTN_RES_KERNEL_STREAM;
       plan.shape = kAnyWidthStreamShape;
-      plan.split = static_cast<int>(H / attn_res_dev::kRtCols);
+      plan.split = kc;
     } else {
       plan.kernel = ATTN_RES_KERNEL_GENERIC;
     }
@@ -432,9 +437,10 @@ attn_res_status_t run(int64_t H, attn_res_bf16_t* prefix, const attn_res_bf16_t*
       if (fn == nullptr) return ATTN_RES_EINVAL;
       e = fn(p, T, H, pdl, static_cast<cudaStream_t>(stream));
     } else if (plan.kernel == ATTN_RES_KERNEL_SPLIT) {
-      LaunchFn fn = lookup(num_blocks, split_index(plan.split), has_delta, has_onorm);
+      const int idx = H == kH ? split_index(plan.split) : kAnyWidthSplitIndex;
+      LaunchFn fn = lookup(num_blocks, idx, has_delta, has_onorm);
       if (fn == nullptr) return ATTN_RES_EINVAL;
-      e = fn(p, T, pdl, static_cast<cudaStream_t>(stream), dev);
+      e = fn(p, T, pdl, static_cast<cudaStream_t>(stream), dev, plan.split);
     } else {
       StreamLaunchFn fn = lookup_stream(num_blocks, plan.shape, has_delta, has_onorm);
       if (fn == nullptr) return ATTN_RES_EINVAL;

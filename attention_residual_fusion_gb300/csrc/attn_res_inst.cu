@@ -28,6 +28,7 @@ LaunchFn ATTN_RES_CAT(launcher_s, ATTN_RES_S)(int split_idx, bool d, bool o) {
     case 2: return pick<kSplits[2]>(d, o);
     case 3: return pick<kSplits[3]>(d, o);
     case 4: return pick<kSplits[4]>(d, o);
+    case kAnyWidthSplitIndex: return pick<0>(d, o);
     default: return nullptr;
   }
 }

@@ -24,17 +24,21 @@
 
 namespace attn_res_dev {
 
+// K = 0: any width H that is a multiple of 1024 up to 8192 -- H / 1024 CTAs
+// per token row (read from the cluster shape), 1024 columns each.
+constexpr int kSplitRtMaxK = 8;
+
 template <int S, bool HAS_DELTA, bool HAS_ONORM, int K>
 struct SplitCfg {
-  static constexpr int VPC = kNV / K;                   // vectors per CTA
+  static constexpr int VPC = K ? kNV / K : 1024 / kVec;  // vectors per CTA
   static constexpr int THREADS = (VPC + 31) / 32 * 32;  // one vector per thread
   static constexpr int NW = THREADS / 32;
   static constexpr bool FULL = (THREADS == VPC);        // no idle threads
-  using Tok = TokenCfg<S, HAS_DELTA, HAS_ONORM, K, NW>;
+  using Tok = TokenCfg<S, HAS_DELTA, HAS_ONORM, K ? K : kSplitRtMaxK, NW>;
   // CTAs of one token exchange partial sums only when there is a softmax
   // (S > 0) or an output norm; otherwise they run as independent CTAs.
   static constexpr bool COMM = Tok::COMM;
-  static_assert(kNV % K == 0, "split must divide the 896 row vectors");
+  static_assert(K == 0 || kNV % K == 0, "split must divide the 896 row vectors");
   static_assert(THREADS <= 1024, "split too small");
   static_assert(K * NW <= 32, "one lane per mailbox slot");
 };
@@ -52,9 +56,11 @@ __global__ void __launch_bounds__(SplitCfg<S, HAS_DELTA, HAS_ONORM, K>::THREADS)
   const int tid = threadIdx.x;
   const int lane = tid & 31;
   const int warp = tid >> 5;
-  // Without a cluster the K CTAs of a token are ordinary neighbours in x.
-  const uint32_t rank = COMM ? cluster_ctarank() : (blockIdx.x % K);
-  const int64_t t = blockIdx.x / K;
+  // CTAs per token row and 1 / H: constants, or from the cluster shape
+  const Split sp{K ? K : (int)cluster_nctarank(), K ? kInvH : p.inv_h};
+  // Without a cluster the CTAs of a token are ordinary neighbours in x.
+  const uint32_t rank = COMM ? cluster_ctarank() : (blockIdx.x % sp.kc);
+  const int64_t t = blockIdx.x / sp.kc;
   const bool active = C::FULL || tid < C::VPC;
   const int64_t col = (int64_t)(rank * C::VPC + tid) * kVec;
 
@@ -62,7 +68,7 @@ __global__ void __launch_bounds__(SplitCfg<S, HAS_DELTA, HAS_ONORM, K>::THREADS)
     if (tid == 0) {
       mailbox_init(mb);
       fence_mbar_init();
-      mailbox_expect<Tok>(mb, 0, HAS_ONORM, Split{K, kInvH});
+      mailbox_expect<Tok>(mb, 0, HAS_ONORM, sp);
     }
     // Announce this CTA (and its initialised mailboxes) to the cluster; the
     // matching wait, just before the first remote store, guarantees every
@@ -103,9 +109,9 @@ __global__ void __launch_bounds__(SplitCfg<S, HAS_DELTA, HAS_ONORM, K>::THREADS)
     const uint4 pre[1] = {x[S]}, del[1] = {x[ROWS - 1]};
     current_row<HAS_DELTA, 1>(pre, del, c);
   }
-  mix_token<S, HAS_DELTA, HAS_ONORM, K, C::NW, 1>(
+  mix_token<S, HAS_DELTA, HAS_ONORM, (K ? K : kSplitRtMaxK), C::NW, 1>(
       [&](int i, int) { return x[i]; }, q, owv, mb, 0, 0u, rank, warp, lane, p.eps, p.out_eps,
-      failed, p.err, [] {}, c, o, Split{K, kInvH});
+      failed, p.err, [] {}, c, o, sp);
 
   // 4. stores; the write-backs follow every read of this column slice
   if (active) {

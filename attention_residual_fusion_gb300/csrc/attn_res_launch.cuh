@@ -16,11 +16,13 @@ using attn_res_dev::Params;
 
 // Enqueue one specialisation: T token rows, optional PDL, on `stream`.
 using LaunchFn = cudaError_t (*)(const Params&, int64_t T, bool pdl,
-                                 cudaStream_t stream, int device);
+                                 cudaStream_t stream, int device, int kc);
 
-// Supported splits (CTAs per token row), in table order.
+// Supported splits (CTAs per token row), in table order; launcher index
+// kNumSplits is the any-width form (K = 0, kc = H / 1024 CTAs per row).
 constexpr int kSplits[] = {4, 7, 8, 14, 16};
 constexpr int kNumSplits = sizeof(kSplits) / sizeof(kSplits[0]);
+constexpr int kAnyWidthSplitIndex = kNumSplits;
 
 inline int split_index(int k) {
   for (int i = 0; i < kNumSplits; ++i)
@@ -30,10 +32,12 @@ inline int split_index(int k) {
 
 template <int S, bool D, bool O, int K>
 cudaError_t launch_split(const Params& p, int64_t T, bool pdl,
-                         cudaStream_t stream, int device) {
+                         cudaStream_t stream, int device, int kc) {
   using C = attn_res_dev::SplitCfg<S, D, O, K>;
   void (*kern)(Params) = attn_res_dev::attn_res_split_kernel<S, D, O, K>;
-  if (C::COMM && K > 8) {
+  if (K != 0) kc = K;
+  if (kc < 1 || kc > (K ? 16 : attn_res_dev::kSplitRtMaxK)) return cudaErrorInvalidValue;
+  if (C::COMM && kc > 8) {
     // clusters above 8 CTAs are opt-in, per function and device
     static std::atomic<uint64_t> enabled{0};
     const uint64_t bit = 1ull << (device & 63);
@@ -48,7 +52,7 @@ cudaError_t launch_split(const Params& p, int64_t T, bool pdl,
   unsigned n = 0;
   if (C::COMM) {
     attrs[n].id = cudaLaunchAttributeClusterDimension;
-    attrs[n].val.clusterDim.x = K;
+    attrs[n].val.clusterDim.x = kc;
     attrs[n].val.clusterDim.y = 1;
     attrs[n].val.clusterDim.z = 1;
     ++n;
@@ -59,7 +63,7 @@ cudaError_t launch_split(const Params& p, int64_t T, bool pdl,
     ++n;
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(T * K), 1, 1);
+  cfg.gridDim = dim3(static_cast<unsigned>(T * kc), 1, 1);
   cfg.blockDim = dim3(C::THREADS, 1, 1);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;

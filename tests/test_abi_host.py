@@ -238,6 +238,16 @@ def test_any_width_stream_checks(lib):
     kw["out_norm_w"] = 0
     kw["layout"].flags = ar.FLAG_KERNEL(2)           # no exchange: not a stream case
     assert ar.call_raw(**kw, H=4096) == 1
+    # the split kernel's any-width form: up to 8 CTAs per row
+    kw = good_h(8192, T=4)
+    kw["layout"].flags = ar.FLAG_KERNEL(1)
+    if no_gpu:
+        assert ar.call_raw(**kw, H=8192) in (4, 5)
+    kw["layout"].flags = ar.FLAG_KERNEL(1) | ar.FLAG_SPLIT(8)
+    assert ar.call_raw(**kw, H=8192) == 1           # no overrides
+    kw = good_h(9216, T=4)
+    kw["layout"].flags = ar.FLAG_KERNEL(1)
+    assert ar.call_raw(**kw, H=9216) == 1           # 9 CTAs per row
 
 
 # ---- hidden-sharded entry points (host checks only) ----

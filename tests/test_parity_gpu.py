@@ -386,3 +386,18 @@ def test_any_width_stream_forced_small_T_and_groups(H):
     wl = W.make_workload(200, 6, capacity=8, has_delta=True, has_out_norm=True,
                          block_write_idx=7, seed=H + 1, H=H, mixing=True, group=3)
     full_check(wl, tag=f"anywidth_group_H{H}")
+
+
+
+SMALLW = [(H, T, S) for H in (1024, 3072, 8192, 12288) for T in (1, 5, 79) for S in (1, 8)]
+
+
+@pytest.mark.parametrize("H,T,S", SMALLW, ids=[f"H{H}_T{T}_S{S}" for H, T, S in SMALLW])
+def test_any_width_few_tokens(H, T, S):
+    """Few tokens at other widths: the split kernel's any-width form (up to 8
+    CTAs per row), the stream kernel's above that."""
+    wl = W.make_workload(T, S, capacity=9, has_delta=bool(T % 2), has_out_norm=bool(S % 2) or T == 5,
+                         block_write_idx=8 if T != 79 else S - 1, seed=H + T + S, H=H, mixing=True)
+    full_check(wl, tag=f"anywidth_small_H{H}_T{T}_S{S}")
+    if H <= 8192:
+        full_check(wl, tag=f"anywidth_small_split_H{H}_T{T}_S{S}", kernel=ar.KERNEL_SPLIT)
