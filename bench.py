@@ -25,7 +25,8 @@ than L2, so no flush is needed between steps.
              the general kernel, graph replay over rotating input sets
   tp_cells   one rank's kernels of the hidden-sharded (TP8) mixture, both
              exchange forms, all-reduces excluded
-  cpu_baseline  the CPU oracle on a bounded sample of the same workload
+  cpu_baseline  the CPU oracle on a bounded sample of the same workload, on
+             all host cores (and on one core: cpu_baseline_one_core)
 
 ``--impl reference`` times the CPU oracle on the same workload and metric.
 Multi-GPU (torchrun): every rank runs its own copy of the workload on its own
@@ -678,6 +679,10 @@ def run_ours(args, rank, world, local_rank, dist):
         line["cpu_baseline"] = {"value": round(rate, 2), "unit": "tokens/s", "cores": threads,
                                 "kind": "oracle",
                                 "sample": f"first {n} token rows of the same workload, {passes} pass(es), {dt:.1f} s"}
+        rate1, n1, passes1, dt1 = oracle_rate(wl, args.cpu_budget / 2, 1)
+        line["cpu_baseline_one_core"] = {
+            "value": round(rate1, 2), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"first {n1} token rows of the same workload, {passes1} pass(es), {dt1:.1f} s"}
     return line
 
 
