@@ -257,7 +257,13 @@ struct RowArgs {
   bool need_weights = true;  // res_w and rms_w are read
   bool writes = true;        // out, prefix (with delta) and the bank slot are written
   Region extra[2] = {};      // float buffers of the hidden-sharded calls
+  bool extra_spans_ok = true;  // and their extents checked by the caller
 };
+
+// (rows - 1) * stride below 2^61 elements.
+bool span_ok(int64_t rows, int64_t stride) {
+  return rows <= 1 || stride <= (int64_t(1) << 61) / (rows - 1);
+}
 
 // Token rows per bank row (B); 0 in the layout means 1.
 int64_t bank_group(const attn_res_layout_t* L) {
@@ -289,6 +295,10 @@ attn_res_status_t check_rows(const RowArgs& a, Params* p) {
     if (bad_row_stride(bs)) return ATTN_RES_EINVAL;
     if (TB > 1 && (bt < (int64_t)(cap - 1) * bs + H || bt > kMaxStride)) return ATTN_RES_EINVAL;
   }
+  // every extent (rows - 1) * stride must stay far from int64 overflow
+  if (!span_ok(T, pr) || (has_delta && !span_ok(T, dr)) || (a.writes && !span_ok(T, orow)) ||
+      (uses_bank && !span_ok(TB, bt)) || !a.extra_spans_ok)
+    return ATTN_RES_EINVAL;
   if (!aligned16(a.prefix) || (a.need_weights && (!aligned16(a.res_w) || !aligned16(a.rms_w))) ||
       (a.writes && !aligned16(a.out)) || (has_delta && !aligned16(a.delta)) ||
       (has_onorm && !aligned16(a.onw)) || (uses_bank && !aligned16(a.blocks)))
@@ -511,6 +521,7 @@ attn_res_status_t run_tp(int phase, int64_t Hs, int64_t H, attn_res_bf16_t* pref
   a.out = out;
   a.need_weights = phase == 0;
   a.writes = phase == 2;
+  a.extra_spans_ok = span_ok(T, sums_row);
   a.extra[0] = floats_region(sums, T, sums_row, nr, phase == 0);
   a.extra[1] = floats_region(uses_sq ? sq : nullptr, T, 1, 1, phase == 1);
   Params p;

@@ -424,3 +424,15 @@ def test_binding_rejects_host_tensors_and_bad_shapes(lib):
     assert lay.blocks_group == 2 and lay.blocks_token == 8 * Hh and lay.blocks_capacity == 8
     with pytest.raises(ValueError):
         ar.make_layout(p, None, b.transpose(1, 2), None, 0)       # inner stride not 1
+
+
+def test_extents_that_would_overflow_are_rejected(lib):
+    """(rows - 1) x stride far beyond any memory is refused before any
+    address arithmetic could wrap."""
+    kw = good(T=1 << 30)
+    kw["layout"].prefix_row = 1 << 39
+    assert call(**kw) == 1
+    kw = good(T=1 << 30)
+    kw["layout"].blocks_token = 1 << 39
+    assert call(**kw) == 1
+    assert tp_call(0, T=1 << 30, sums_row=1 << 39) == 1
