@@ -227,3 +227,33 @@ def test_chunked_pipeline(gram, chunk, B):
     wl = W.make_workload(61, 8, capacity=9, has_delta=True, has_out_norm=True,
                          block_write_idx=8, seed=80 + chunk, mixing=True, group=B)
     tp_check(wl, [W.HIDDEN // 4] * 4, f"tp_chunk{chunk}", gram=gram, chunk=chunk)
+
+
+def _draw_tp(k: int):
+    rng = np.random.default_rng(30_000 + k)
+    R = int(rng.choice([1, 2, 3, 4, 8]))
+    base = int(rng.choice([8, 64, 896, 1024]))
+    widths = [base * int(rng.integers(1, 5)) for _ in range(R)]
+    H = sum(widths)
+    S = int(rng.integers(0, 9))
+    cap = S + int(rng.integers(1, 3)) if S < 8 else 9
+    group = int(rng.choice([1, 1, 2]))
+    free = list(range(S, cap))
+    widx = int(rng.choice([-1] + free + ([] if group > 1 else list(range(S)))))
+    T = int(rng.choice([1, 3, 17, 64, 130]))
+    chunk = int(rng.choice([0, 0, 2 * group, 8 * group]))
+    return dict(widths=widths, H=H, S=S, cap=cap, group=group, widx=widx, T=T,
+                delta=bool(rng.integers(0, 2)), norm=bool(rng.integers(0, 2)),
+                gram=bool(rng.integers(0, 2)), pdl=bool(rng.integers(0, 2)),
+                chunk=chunk or None, pad=int(rng.choice([0, 8])))
+
+
+@pytest.mark.parametrize("k", range(24))
+def test_random_sharding(k):
+    """Seeded random shardings (rank count, uneven widths, any H), variants,
+    shared rows, both exchange forms, PDL and chunking, against the oracle."""
+    c = _draw_tp(k)
+    wl = W.make_workload(c["T"], c["S"], capacity=c["cap"], has_delta=c["delta"],
+                         has_out_norm=c["norm"], block_write_idx=c["widx"], seed=31_000 + k,
+                         H=c["H"], mixing=True, slot_stride=c["H"] + c["pad"], group=c["group"])
+    tp_check(wl, c["widths"], f"tp_random_{c}", gram=c["gram"], pdl=c["pdl"], chunk=c["chunk"])
