@@ -195,6 +195,21 @@ TpLaunchFn lookup_tp(int S, int phase, bool d, bool o, bool g) {
   }
 }
 
+TpRingLaunchFn lookup_tp_ring(int S, int phase, bool d, bool o, bool g) {
+  switch (S) {
+    case 0: return tp_ring_launcher_s0(phase, d, o, g);
+    case 1: return tp_ring_launcher_s1(phase, d, o, g);
+    case 2: return tp_ring_launcher_s2(phase, d, o, g);
+    case 3: return tp_ring_launcher_s3(phase, d, o, g);
+    case 4: return tp_ring_launcher_s4(phase, d, o, g);
+    case 5: return tp_ring_launcher_s5(phase, d, o, g);
+    case 6: return tp_ring_launcher_s6(phase, d, o, g);
+    case 7: return tp_ring_launcher_s7(phase, d, o, g);
+    case 8: return tp_ring_launcher_s8(phase, d, o, g);
+    default: return nullptr;
+  }
+}
+
 StreamLaunchFn lookup_stream(int S, int shape, bool d, bool o) {
   switch (S) {
     case 0: return stream_launcher_s0(shape, d, o);
@@ -480,6 +495,43 @@ int tp_threads(int64_t Hs, int cap) {
   return static_cast<int>(nv >= cap ? cap : ((nv + 31) / 32) * 32);
 }
 
+// Form of the hidden-sharded kernels: the persistent ring when `stages`
+// stages of a token's rows (and, for the sums, the query rows) fit in
+// kTpRingMaxSmem bytes and there are at least
+// kTpRingMinTokens rows (or when forced with ATTN_RES_KERNEL_STREAM), else
+// one CTA per row (forced with ATTN_RES_KERNEL_GENERIC).  Ring depth 2 (a
+// deeper ring fits fewer CTAs per SM and measured slower at every size);
+// ATTN_RES_FLAG_STAGES(2..4) overrides it when the ring runs, and is an
+// error together with ATTN_RES_KERNEL_GENERIC.  *stages = -1
+// for an override that cannot be met (ATTN_RES_EINVAL).
+// below ~1024 rows the ring's CTAs get one or two tokens each and its setup
+// costs more than it saves (measured on TP8 shards of 896 columns)
+constexpr int64_t kTpRingMinTokens = 1024;
+bool tp_ring_plan(int phase, bool gram, int64_t T, int64_t Hs, int num_blocks, bool has_delta,
+                  uint32_t flags, int threads, int* stages) {
+  const int forced = static_cast<int>((flags >> 16) & 0xfu);
+  const int want = static_cast<int>((flags >> 20) & 0xfu);
+  const int rows = num_blocks + 1 + (has_delta ? 1 : 0);
+  auto fits = [&](int st) {
+    return attn_res_dev::tp_ring_smem_bytes(rows, Hs, st, phase == 0 && gram, threads) <= kTpRingMaxSmem;
+  };
+  *stages = 0;
+  if ((forced != 0 && forced != ATTN_RES_KERNEL_STREAM && forced != ATTN_RES_KERNEL_GENERIC) ||
+      (want != 0 && (want < 2 || want > attn_res_dev::kTpRingMaxStages))) {
+    *stages = -1;
+    return false;
+  }
+  bool ring = forced == ATTN_RES_KERNEL_STREAM ||
+              (forced == 0 && T >= kTpRingMinTokens && fits(want ? want : 2));
+  if (!ring) {
+    if (want != 0 && forced == ATTN_RES_KERNEL_GENERIC) *stages = -1;  // a depth without the ring
+    return false;
+  }
+  *stages = want ? want : 2;
+  if (!fits(*stages)) *stages = -1;
+  return *stages > 0;
+}
+
 // One phase of the hidden-sharded mixture: shared checks and launch.
 // phase 0 reads the rows and weights and writes sums; phase 1 reads the rows
 // and sums and writes sq; phase 2 reads the rows, sums and (with an output
@@ -491,12 +543,19 @@ attn_res_status_t run_tp(int phase, int64_t Hs, int64_t H, attn_res_bf16_t* pref
                          const attn_res_bf16_t* out_norm_w, float eps, float out_eps, float* sums,
                          int64_t sums_row, float* sq, attn_res_bf16_t* out, int64_t T,
                          const attn_res_layout_t* layout, void* stream) {
-  // the sharded kernels have one launch shape: only PDL and TP_GRAM apply
+  // PDL, TP_GRAM, and the kernel form and ring depth overrides apply
   attn_res_status_t st = check_scalars(T, Hs, num_blocks, block_write_idx, eps, out_eps, layout,
-                                       ATTN_RES_FLAG_PDL | ATTN_RES_FLAG_TP_GRAM);
+                                       ATTN_RES_FLAG_PDL | ATTN_RES_FLAG_TP_GRAM |
+                                           ATTN_RES_FLAG_KERNEL(0xf) | ATTN_RES_FLAG_STAGES(0xf));
   if (st != ATTN_RES_OK) return st;
   const bool gram = (layout->flags & ATTN_RES_FLAG_TP_GRAM) != 0;
   if (phase == 1 && gram) return ATTN_RES_EINVAL;  // the Gram form has no sq phase
+  const int threads = tp_threads(Hs, (phase == 0 && gram) ? attn_res_dev::kTpGramThreads
+                                                          : attn_res_dev::kTpMaxThreads);
+  int stages = 0;
+  const bool ring =
+      tp_ring_plan(phase, gram, T, Hs, num_blocks, delta != nullptr, layout->flags, threads, &stages);
+  if (stages < 0) return ATTN_RES_EINVAL;
   const int nr = attn_res_tp_sums_width(num_blocks, gram ? 1 : 0);
   if (H < Hs || H > kMaxStride || sums_row < nr || sums_row > kMaxStride) return ATTN_RES_EINVAL;
   if (T > INT32_MAX) return ATTN_RES_EINVAL;
@@ -538,14 +597,19 @@ attn_res_status_t run_tp(int phase, int64_t Hs, int64_t H, attn_res_bf16_t* pref
   ta.sums = sums;
   ta.sums_row = sums_row;
   ta.sq = uses_sq ? sq : nullptr;
-  TpLaunchFn fn = lookup_tp(num_blocks, phase, delta != nullptr, onorm, gram);
-  if (fn == nullptr) return ATTN_RES_EINVAL;
-  const int threads = tp_threads(Hs, (phase == 0 && gram) ? attn_res_dev::kTpGramThreads
-                                                          : attn_res_dev::kTpMaxThreads);
+  const bool pdl = (layout->flags & ATTN_RES_FLAG_PDL) != 0;
   cudaError_t e = status_word(dev, &p.err);
-  if (e == cudaSuccess)
-    e = fn(p, ta, T, threads, (layout->flags & ATTN_RES_FLAG_PDL) != 0,
-           static_cast<cudaStream_t>(stream));
+  if (e == cudaSuccess) {
+    if (ring) {
+      TpRingLaunchFn fn = lookup_tp_ring(num_blocks, phase, delta != nullptr, onorm, gram);
+      if (fn == nullptr) return ATTN_RES_EINVAL;
+      e = fn(p, ta, T, threads, stages, pdl, static_cast<cudaStream_t>(stream), dev);
+    } else {
+      TpLaunchFn fn = lookup_tp(num_blocks, phase, delta != nullptr, onorm, gram);
+      if (fn == nullptr) return ATTN_RES_EINVAL;
+      e = fn(p, ta, T, threads, pdl, static_cast<cudaStream_t>(stream));
+    }
+  }
   if (e != cudaSuccess) {
     (void)cudaGetLastError();
     return ATTN_RES_ECUDA;

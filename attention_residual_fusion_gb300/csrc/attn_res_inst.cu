@@ -87,4 +87,21 @@ TpLaunchFn ATTN_RES_CAT(tp_launcher_s, ATTN_RES_S)(int phase, bool d, bool o, bo
   }
 }
 
+template <int S, bool D>
+TpRingLaunchFn tp_ring_fn(int phase, bool o, bool g) {
+  switch (phase) {
+    case 0: return g ? &launch_tp_ring<S, D, 0, false, true> : &launch_tp_ring<S, D, 0, false, false>;
+    case 1: return &launch_tp_ring<S, D, 1, true, false>;
+    case 2:
+      if (o) return g ? &launch_tp_ring<S, D, 2, true, true> : &launch_tp_ring<S, D, 2, true, false>;
+      return &launch_tp_ring<S, D, 2, false, false>;  // without an output norm GRAM changes nothing
+    default: return nullptr;
+  }
+}
+
+TpRingLaunchFn ATTN_RES_CAT(tp_ring_launcher_s, ATTN_RES_S)(int phase, bool d, bool o, bool g) {
+  constexpr int S = ATTN_RES_S;
+  return d ? tp_ring_fn<S, true>(phase, o, g) : tp_ring_fn<S, false>(phase, o, g);
+}
+
 }  // namespace attn_res_host

@@ -38,7 +38,7 @@ struct SplitCfg {
   // CTAs of one token exchange partial sums only when there is a softmax
   // (S > 0) or an output norm; otherwise they run as independent CTAs.
   static constexpr bool COMM = Tok::COMM;
-  static_assert(K == 0 || kNV % K == 0, "split must divide the 896 row vectors");
+  static_assert(kNV % (K ? K : 1) == 0, "split must divide the 896 row vectors");
   static_assert(THREADS <= 1024, "split too small");
   static_assert(K * NW <= 32, "one lane per mailbox slot");
 };

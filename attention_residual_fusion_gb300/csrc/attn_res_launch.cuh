@@ -227,6 +227,62 @@ cudaError_t launch_tp_finish(const Params& p, const TpArgs& a, int64_t T, int th
   return launch_tp(attn_res_dev::attn_res_tp_finish_kernel<S, D, O, G>, p, a, T, th, pdl, s);
 }
 
+// Hidden-sharded phases, persistent ring form: CTAs per SM x SMs CTAs (at
+// most T), each with a `stages`-deep ring of its tokens' rows in dynamic
+// shared memory.
+using TpRingLaunchFn = cudaError_t (*)(const Params&, const TpArgs&, int64_t T, int threads,
+                                       int stages, bool pdl, cudaStream_t stream, int device);
+
+// bytes of one CTA's dynamic shared memory, at most (the kernel's static
+// shared memory stays under 2 KB: within the 227 KB a CTA may have)
+constexpr int kTpRingMaxSmem = 220 * 1024;
+
+template <int S, bool D, int PH, bool O, bool G>
+cudaError_t launch_tp_ring(const Params& p, const TpArgs& a, int64_t T, int threads, int stages,
+                           bool pdl, cudaStream_t stream, int device) {
+  using C = attn_res_dev::TpRingCfg<S, D, PH, O, G>;
+  void (*kern)(Params, TpArgs, int) = attn_res_dev::attn_res_tp_ring_kernel<S, D, PH, O, G>;
+  if (device < 0 || device >= 64 || stages < 2 || stages > attn_res_dev::kTpRingMaxStages ||
+      threads < 32 || threads > C::THREADS_MAX || threads % 32)
+    return cudaErrorInvalidValue;
+  const int64_t smem = attn_res_dev::tp_ring_smem_bytes(C::ROWS, a.Hs, stages, PH == 0 && G, threads);
+  if (smem > kTpRingMaxSmem) return cudaErrorInvalidValue;
+  // per device: the attribute set once, and the last (shared memory,
+  // threads) -> CTAs per SM x SMs answer, packed as key << 20 | CTAs
+  static std::atomic<bool> attr_set[64];
+  static std::atomic<uint64_t> resident[64];
+  if (!attr_set[device].load(std::memory_order_acquire)) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kTpRingMaxSmem);
+    if (e != cudaSuccess) return e;
+    attr_set[device].store(true, std::memory_order_release);
+  }
+  const uint64_t key = ((uint64_t)smem << 10) | (uint64_t)threads;
+  uint64_t r = resident[device].load(std::memory_order_acquire);
+  int64_t ctas = (r >> 20) == key ? (int64_t)(r & 0xfffffu) : 0;
+  if (ctas == 0) {
+    int per_sm = 0, sms = 0;
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, (size_t)smem);
+    if (e != cudaSuccess) return e;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
+    if (e != cudaSuccess) return e;
+    ctas = (int64_t)per_sm * sms;
+    if (ctas < 1 || ctas > 0xfffff) return cudaErrorInvalidConfiguration;
+    resident[device].store((key << 20) | (uint64_t)ctas, std::memory_order_release);
+  }
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(T < ctas ? T : ctas), 1, 1);
+  cfg.blockDim = dim3(static_cast<unsigned>(threads), 1, 1);
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+  cfg.stream = stream;
+  cfg.attrs = &attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, p, a, stages);
+}
+
 // One row of the table per num_blocks, defined in attn_res_inst.cu (compiled
 // once per S).  Returns nullptr for an unknown split index.
 LaunchFn launcher_s0(int split_idx, bool has_delta, bool has_onorm);
@@ -269,5 +325,14 @@ TpLaunchFn tp_launcher_s5(int phase, bool d, bool o, bool g);
 TpLaunchFn tp_launcher_s6(int phase, bool d, bool o, bool g);
 TpLaunchFn tp_launcher_s7(int phase, bool d, bool o, bool g);
 TpLaunchFn tp_launcher_s8(int phase, bool d, bool o, bool g);
+TpRingLaunchFn tp_ring_launcher_s0(int phase, bool d, bool o, bool g);
+TpRingLaunchFn tp_ring_launcher_s1(int phase, bool d, bool o, bool g);
+TpRingLaunchFn tp_ring_launcher_s2(int phase, bool d, bool o, bool g);
+TpRingLaunchFn tp_ring_launcher_s3(int phase, bool d, bool o, bool g);
+TpRingLaunchFn tp_ring_launcher_s4(int phase, bool d, bool o, bool g);
+TpRingLaunchFn tp_ring_launcher_s5(int phase, bool d, bool o, bool g);
+TpRingLaunchFn tp_ring_launcher_s6(int phase, bool d, bool o, bool g);
+TpRingLaunchFn tp_ring_launcher_s7(int phase, bool d, bool o, bool g);
+TpRingLaunchFn tp_ring_launcher_s8(int phase, bool d, bool o, bool g);
 
 }  // namespace attn_res_host

@@ -29,8 +29,8 @@ from __future__ import annotations
 
 import types
 
-from . import (AttnResError, FLAG_PDL, FLAG_TP_GRAM, _ptr, check_bf16_cuda, lib, make_layout,
-               status_string)
+from . import (AttnResError, FLAG_KERNEL, FLAG_PDL, FLAG_STAGES, FLAG_TP_GRAM, _ptr,
+               check_bf16_cuda, lib, make_layout, status_string)
 
 
 def sums_width(num_blocks: int, gram: bool = False) -> int:
@@ -39,8 +39,12 @@ def sums_width(num_blocks: int, gram: bool = False) -> int:
     return 2 * n + (n * (n - 1) // 2 if gram else 0)
 
 
-def _flags(pdl: bool, gram: bool) -> int:
-    return (FLAG_PDL if pdl else 0) | (FLAG_TP_GRAM if gram else 0)
+def _flags(pdl: bool, gram: bool, kernel: int = 0, stages: int = 0) -> int:
+    """Layout flags of a sharded call.  ``kernel``: 0 automatic,
+    KERNEL_STREAM the persistent ring form, KERNEL_GENERIC one CTA per token
+    row; ``stages``: ring depth 2..4 (0 automatic)."""
+    return ((FLAG_PDL if pdl else 0) | (FLAG_TP_GRAM if gram else 0) | FLAG_KERNEL(kernel) |
+            FLAG_STAGES(stages))
 
 
 def _stream_handle(stream, device) -> int:
@@ -65,12 +69,13 @@ def _raise(st: int) -> None:
 
 
 def tp_sums(prefix, delta, blocks, num_blocks: int, res_w, rms_w, sums, *,
-            gram: bool = False, pdl: bool = False, blocks_group: int = 1, stream=None) -> None:
+            gram: bool = False, pdl: bool = False, blocks_group: int = 1, kernel: int = 0,
+            stages: int = 0, stream=None) -> None:
     """attn_res_tp_sums on the shard: sums[t, :2N] = (sum x_i^2, <x_i, q>),
     then the Gram entries with ``gram``."""
     check_bf16_cuda(prefix=prefix, delta=delta, blocks=blocks, res_w=res_w, rms_w=rms_w)
     _check_f32_cuda(sums=sums)
-    lay = make_layout(prefix, delta, blocks, None, _flags(pdl, gram), blocks_group)
+    lay = make_layout(prefix, delta, blocks, None, _flags(pdl, gram, kernel, stages), blocks_group)
     _raise(lib().attn_res_tp_sums(
         res_w.shape[0], _ptr(prefix) or None, _ptr(delta) or None, _ptr(blocks) or None,
         num_blocks, _ptr(res_w) or None, _ptr(rms_w) or None, _ptr(sums) or None,
@@ -78,11 +83,12 @@ def tp_sums(prefix, delta, blocks, num_blocks: int, res_w, rms_w, sums, *,
 
 
 def tp_sq(prefix, delta, blocks, num_blocks: int, H: int, eps: float, sums, sq, *,
-          pdl: bool = False, blocks_group: int = 1, stream=None) -> None:
+          pdl: bool = False, blocks_group: int = 1, kernel: int = 0, stages: int = 0,
+          stream=None) -> None:
     """attn_res_tp_sq on the shard: sq[t] = sum over the shard of acc^2."""
     check_bf16_cuda(prefix=prefix, delta=delta, blocks=blocks)
     _check_f32_cuda(sums=sums, sq=sq)
-    lay = make_layout(prefix, delta, blocks, None, FLAG_PDL if pdl else 0, blocks_group)
+    lay = make_layout(prefix, delta, blocks, None, _flags(pdl, False, kernel, stages), blocks_group)
     _raise(lib().attn_res_tp_sq(
         prefix.shape[1], H, _ptr(prefix) or None, _ptr(delta) or None, _ptr(blocks) or None,
         num_blocks, eps, _ptr(sums) or None, sums.stride(0), _ptr(sq) or None,
@@ -91,12 +97,12 @@ def tp_sq(prefix, delta, blocks, num_blocks: int, H: int, eps: float, sums, sq, 
 
 def tp_finish(prefix, delta, blocks, num_blocks: int, block_write_idx: int, H: int,
               out_norm_w, eps: float, out_eps: float, sums, sq, out, *,
-              gram: bool = False, pdl: bool = False, blocks_group: int = 1,
-              stream=None) -> None:
+              gram: bool = False, pdl: bool = False, blocks_group: int = 1, kernel: int = 0,
+              stages: int = 0, stream=None) -> None:
     """attn_res_tp_finish on the shard: out and the write-backs of c."""
     check_bf16_cuda(prefix=prefix, delta=delta, blocks=blocks, out_norm_w=out_norm_w, out=out)
     _check_f32_cuda(sums=sums, sq=sq)
-    lay = make_layout(prefix, delta, blocks, out, _flags(pdl, gram), blocks_group)
+    lay = make_layout(prefix, delta, blocks, out, _flags(pdl, gram, kernel, stages), blocks_group)
     _raise(lib().attn_res_tp_finish(
         prefix.shape[1], H, _ptr(prefix) or None, _ptr(delta) or None, _ptr(blocks) or None,
         num_blocks, block_write_idx, _ptr(out_norm_w) or None, eps, out_eps,
@@ -111,7 +117,7 @@ def attn_res_tp(prefix, delta, blocks, num_blocks: int, block_write_idx: int, re
                 out_norm_w=None, eps: float = 1e-6, out_eps: float = 1e-6, out=None, *,
                 H: int | None = None, group=None, all_reduce=None, phases=None,
                 gram: bool = False, pdl: bool = False, blocks_group: int = 1,
-                chunk_tokens: int | None = None, stream=None):
+                chunk_tokens: int | None = None, kernel: int = 0, stages: int = 0, stream=None):
     """The mixture on this rank's column shard (every row-sized argument is
     the shard, width ``res_w.shape[0]``).  ``H`` is the full width (default:
     shard width x world size of ``group``).  ``all_reduce(tensor)`` sums a
@@ -119,7 +125,8 @@ def attn_res_tp(prefix, delta, blocks, num_blocks: int, block_write_idx: int, re
     ``wait()`` (default: torch.distributed's asynchronous all_reduce on
     ``group``; with no process group initialised the call is local).
     ``gram`` selects the single-exchange form; ``blocks_group`` as for
-    attn_res.
+    attn_res; ``kernel`` and ``stages`` pick the kernels' form (see
+    ``_flags``; results do not depend on it beyond fp32 summation order).
 
     ``chunk_tokens`` runs the token rows in chunks, software-pipelined: the
     first kernel of chunk c+1 is issued while the all-reduce of chunk c is in
@@ -138,7 +145,7 @@ def attn_res_tp(prefix, delta, blocks, num_blocks: int, block_write_idx: int, re
     with ctx:
         return _attn_res_tp(prefix, delta, blocks, num_blocks, block_write_idx, res_w, rms_w,
                             out_norm_w, eps, out_eps, out, H, group, all_reduce, phases, gram,
-                            pdl, blocks_group, chunk_tokens, stream)
+                            pdl, blocks_group, chunk_tokens, kernel, stages, stream)
 
 
 def _wait(handle) -> None:
@@ -148,7 +155,7 @@ def _wait(handle) -> None:
 
 def _attn_res_tp(prefix, delta, blocks, num_blocks, block_write_idx, res_w, rms_w, out_norm_w,
                  eps, out_eps, out, H, group, all_reduce, phases, gram, pdl, blocks_group,
-                 chunk_tokens, stream):
+                 chunk_tokens, kernel, stages, stream):
     import torch
     import torch.distributed as dist
 
@@ -182,6 +189,8 @@ def _attn_res_tp(prefix, delta, blocks, num_blocks, block_write_idx, res_w, rms_
     kw = dict(pdl=pdl, stream=stream)
     if B != 1:
         kw["blocks_group"] = B
+    if kernel or stages:
+        kw.update(kernel=kernel, stages=stages)
 
     bounds = [(c0, min(T, c0 + chunk)) for c0 in range(0, T, chunk)] or [(0, 0)]
 

@@ -340,9 +340,20 @@ def sweep_prefill(ar, torch, dev, stream, peak):
 WIDTHS = ["width:4096:2048:8", "width:8192:2048:8"]
 
 
+def width_kernel(wl) -> str:
+    """Kernel attn_res_h runs for the workload's width (the routing its
+    header documents): multiples of 1024 with a row exchange take the
+    any-width split (T < 80) or stream form, every other width the general
+    kernel."""
+    exchange = wl.num_blocks > 0 or wl.out_norm_w is not None
+    if wl.H % 1024 == 0 and exchange and wl.H // 1024 <= 16:
+        return "any-width split" if wl.T < 80 and wl.H // 1024 <= 8 else "any-width stream"
+    return "general"
+
+
 def width_cells(ar, torch, dev, stream, peak):
-    """Other model widths (the general kernel behind attn_res_h): µs per call
-    from graph replay over rotating input sets larger than 3x L2."""
+    """Other model widths through attn_res_h: µs per call from graph replay
+    over rotating input sets larger than 3x L2."""
     rows = []
     for name in WIDTHS:
         wl, _ = make(name)
@@ -350,7 +361,7 @@ def width_cells(ar, torch, dev, stream, peak):
         sets = input_sets(wl, t, torch, dev)
         us = time_graph(ar, wl, sets, torch, stream)
         gbs = wl.algorithmic_bytes() / (us * 1e-6) / 1e9
-        rows.append({"workload": name, "kernel": "general", "us_per_call": round(us, 2),
+        rows.append({"workload": name, "kernel": width_kernel(wl), "us_per_call": round(us, 2),
                      "tokens_per_s": round(wl.T / (us * 1e-6), 1), "gbs": round(gbs, 1),
                      "frac": round(gbs / peak, 4), "input_sets": len(sets)})
         del t, sets
@@ -365,7 +376,8 @@ def tp_cells(ar, torch, dev, stream, peak, ranks=8):
     all-reduces between the kernels are not part of the number (one GPU:
     there is nothing to exchange with); `kernels` says how many launches a
     step makes.  `frac` = single-pass algorithmic bytes of the shard per
-    step / time, against the measured copy bandwidth."""
+    step / time, against the measured copy bandwidth; `frac_all_passes` the
+    same with the bytes of every pass (each re-reads the rows)."""
     from attention_residual_fusion_gb300 import tp
     rows = []
     for name in ("long_prefill", "single_token"):
@@ -412,11 +424,17 @@ def tp_cells(ar, torch, dev, stream, peak, ranks=8):
             form = "single exchange (Gram)" if gram else "two exchanges"
             if chunk:
                 form += f", pipelined chunks of {chunk} rows"
+            # every pass reads the token's rows again; the last also writes
+            passes = 2 if gram else 3
+            row_reads = wl.T * (wl.num_blocks + 1 + int(wl.delta is not None)) * Hs * 2
+            moved = alg + (passes - 1) * row_reads
             rows.append({"workload": f"{name} shard 1/{ranks} (H_s={Hs})", "form": form,
                          "kernels": (2 if gram else 3) * nch,
                          "all_reduces": (1 if gram else 2) * nch,
                          "us_per_step": round(us, 3), "tokens_per_s": round(wl.T / (us * 1e-6), 1),
                          "gbs": round(gbs, 1), "frac": round(gbs / peak, 4),
+                         "passes": passes, "bytes_all_passes": moved,
+                         "frac_all_passes": round(moved / (us * 1e-6) / 1e9 / peak, 4),
                          "input_sets": len(sets)})
         del sets, shard
         torch.cuda.empty_cache()

@@ -265,7 +265,7 @@ def tp_call(phase, T=4, S=4, Hs=HS, Hfull=H, sums_row=None, sums=None, sq=None, 
     import ctypes
 
     L = ar.lib()
-    lay = tp_layout(T=T, flags=flags)
+    lay = tp_layout(T=T, flags=flags, W=max(Hs, HS))
     p = dict(prefix=addr(0), delta=addr(1), blocks=addr(2), res_w=addr(3), rms_w=addr(4),
              onw=addr(5) if onorm else 0, out=addr(6))
     p.update(ptrs)
@@ -304,11 +304,34 @@ def test_tp_valid_arguments_reach_the_device_check(lib, phase):
     (dict(sums=0), 1),
     (dict(sums=addr(7, 2)), 2),              # floats want 4-byte alignment
     (dict(prefix=addr(0, 8)), 2),
-    (dict(flags=ar.FLAG_SPLIT(7)), 1),       # one launch shape: only PDL
-    (dict(flags=ar.FLAG_KERNEL(2)), 1),
+    (dict(flags=ar.FLAG_SPLIT(7)), 1),       # no split or vector overrides
+    (dict(flags=ar.FLAG_VPT(2)), 1),
+    (dict(flags=ar.FLAG_KERNEL(1)), 1),      # forms: ring (2) or one CTA per row (3)
+    (dict(flags=ar.FLAG_KERNEL(4)), 1),
+    (dict(flags=ar.FLAG_STAGES(1)), 1),      # ring depth 2..4
+    (dict(flags=ar.FLAG_STAGES(5)), 1),
+    (dict(flags=ar.FLAG_KERNEL(3) | ar.FLAG_STAGES(2)), 1),   # a depth without the ring
+    # a forced ring whose stages do not fit in shared memory (2 x 6 rows x 32 KB)
+    (dict(flags=ar.FLAG_KERNEL(2), Hs=16384, Hfull=16384), 1),
 ])
 def test_tp_rejections(lib, phase, change, status):
     assert tp_call(phase, **change) == status
+
+
+@pytest.mark.parametrize("phase", [0, 1, 2])
+@pytest.mark.parametrize("flags", [ar.FLAG_KERNEL(2), ar.FLAG_KERNEL(3),
+                                   ar.FLAG_KERNEL(2) | ar.FLAG_STAGES(2),
+                                   ar.FLAG_KERNEL(2) | ar.FLAG_STAGES(4), ar.FLAG_STAGES(3)])
+def test_tp_form_overrides_accepted(lib, phase, flags):
+    """Both forms and the ring depths 2..4 pass the host checks (then the
+    device check, without a GPU); a depth with the automatic form at few
+    rows (one CTA per row) does not apply.  A wide shard falls back to one
+    CTA per row unless the ring is forced."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a device is present")
+    assert tp_call(phase, flags=flags) in (4, 5)
+    assert tp_call(phase, Hs=16384, Hfull=16384) in (4, 5)
 
 
 def test_tp_phase_specific_rejections(lib):

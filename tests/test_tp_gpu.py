@@ -56,7 +56,8 @@ class ThreadGroup:
         return fn
 
 
-def run_tp_ranks(wl: W.Workload, widths, *, pdl=False, out_row=None, gram=False, chunk=None):
+def run_tp_ranks(wl: W.Workload, widths, *, pdl=False, out_row=None, gram=False, chunk=None,
+                 kernel=0, stages=0):
     """Run attn_res_tp on every column shard (one thread per rank) over guarded
     device copies of the workload; return host copies like gpu_util.run_gpu."""
     import torch
@@ -86,7 +87,8 @@ def run_tp_ranks(wl: W.Workload, widths, *, pdl=False, out_row=None, gram=False,
                     g_res.view[a:b], g_rms.view[a:b],
                     None if g_onw is None else g_onw.view[a:b], wl.eps, wl.out_eps,
                     g_out.view[:, a:b], H=H, all_reduce=group.all_reduce_for(r), gram=gram,
-                    pdl=pdl, blocks_group=wl.group, chunk_tokens=chunk, stream=stream)
+                    pdl=pdl, blocks_group=wl.group, chunk_tokens=chunk, kernel=kernel,
+                    stages=stages, stream=stream)
         except BaseException as e:  # noqa: BLE001 - reported below
             errors.append(e)
             group.barrier.abort()
@@ -123,14 +125,45 @@ CASES = [(R, S, d, o, w, g) for R in (1, 2, 8) for S in (0, 1, 4, 8)
          for (d, o, w) in ((True, True, 8), (False, True, -1), (True, False, "S"), (False, False, -1))
          for g in (False, True) if o or not g]
 
+# kernel forms: automatic (the ring from 1024 rows where it fits), one CTA per
+# row, the ring
+FORMS = {"auto": {}, "rows": dict(kernel=ar.KERNEL_GENERIC), "ring": dict(kernel=ar.KERNEL_STREAM)}
 
+
+@pytest.mark.parametrize("form", ["ring", "rows"])
 @pytest.mark.parametrize("R,S,d,o,w,g", CASES,
                          ids=[f"R{R}_S{S}_d{int(d)}_o{int(o)}_w{w}_g{int(g)}" for R, S, d, o, w, g in CASES])
-def test_even_shards(R, S, d, o, w, g):
+def test_even_shards(R, S, d, o, w, g, form):
     widx = S if w == "S" else w
     wl = W.make_workload(37, S, capacity=9, has_delta=d, has_out_norm=o, block_write_idx=widx,
                          seed=500 + 10 * R + S, mixing=True)
-    tp_check(wl, [W.HIDDEN // R] * R, f"tp_R{R}_S{S}_g{int(g)}", gram=g)
+    widths = [W.HIDDEN // R] * R
+    if form == "ring" and not ring_fits(widths[0], S, d, g and o):
+        with pytest.raises(ar.AttnResError):   # a forced ring that does not fit is refused
+            run_tp_ranks(wl, widths, gram=g, **FORMS[form])
+        return
+    tp_check(wl, widths, f"tp_R{R}_S{S}_g{int(g)}_{form}", gram=g, **FORMS[form])
+
+
+def ring_fits(Hs, S, delta, gram, stages=2):
+    """Whether every phase's ring of an Hs-wide shard fits the library's 220 KB
+    (stages of rows at a 16-byte padded pitch; the Gram sums also hold two
+    query rows, 16 bytes and two 16 x 16 fp32 tiles per warp)."""
+    rows = S + 1 + int(delta)
+    warps = min(-(-Hs // 8 // 32), 128 // 32)
+    ring = stages * rows * (Hs * 2 + 16)
+    return ring + (4 * Hs + 16 + 2 * warps * 1024 if gram else 0) <= 220 * 1024
+
+
+@pytest.mark.parametrize("stages", [2, 3, 4])
+@pytest.mark.parametrize("gram", [False, True])
+def test_ring_wraps(stages, gram):
+    """More token rows than resident CTAs: each CTA of the ring form walks
+    several tokens and reuses every stage (1500 rows over ~600 CTAs of an
+    896-column shard), full oracle comparison, eight shards."""
+    wl = W.make_workload(1500, 8, capacity=9, has_delta=True, has_out_norm=True,
+                         block_write_idx=8, seed=900 + stages, mixing=True, outliers=True)
+    tp_check(wl, [896] * 8, f"tp_ring{stages}", gram=gram, kernel=ar.KERNEL_STREAM, stages=stages)
 
 
 @pytest.mark.parametrize("gram", [False, True])
@@ -141,13 +174,26 @@ def test_uneven_shards(widths, gram):
     tp_check(wl, widths, f"tp_uneven_{len(widths)}", gram=gram)
 
 
+@pytest.mark.parametrize("form", ["ring", "rows"])
 @pytest.mark.parametrize("H,widths", [(64, [8, 56]), (200, [96, 104]), (1024, [256] * 4),
-                                     (4096, [2048] * 2), (16384, [4096] * 4)])
-def test_other_widths(H, widths):
+                                     (4096, [2048] * 2), (16384, [4096] * 4), (16384, [16384])])
+def test_other_widths(H, widths, form):
+    """Any width.  The 16384-wide single shard does not fit a ring (6 rows x
+    32 KB x 2 stages > 200 KB): forcing the ring is refused, and at 1100
+    rows the automatic form falls back to one CTA per row."""
     wl = W.make_workload(23, 4, capacity=5, has_delta=True, has_out_norm=True,
                          block_write_idx=4, seed=H, H=H, mixing=True, slot_stride=H + 8)
-    tp_check(wl, widths, f"tp_H{H}")
-    tp_check(wl, widths, f"tp_H{H}_gram", gram=True)
+    if form == "ring" and max(widths) == 16384:
+        with pytest.raises(ar.AttnResError):
+            run_tp_ranks(wl, widths, **FORMS[form])
+        wl = W.make_workload(1100, 4, capacity=5, has_delta=True, has_out_norm=True,
+                             block_write_idx=4, seed=H, H=H, mixing=True)
+        idx = np.sort(np.random.default_rng(5).choice(wl.T, 12, replace=False))
+        ref = oracle.run_workload(wl, n_threads=NT, tokens=idx)
+        G.check_against_oracle(wl, run_tp_ranks(wl, widths), ref, tokens=idx, tag="tp_wide_auto")
+        return
+    tp_check(wl, widths, f"tp_H{H}_{form}", **FORMS[form])
+    tp_check(wl, widths, f"tp_H{H}_gram_{form}", gram=True, **FORMS[form])
 
 
 def test_pdl_and_padded_rows():
@@ -242,10 +288,25 @@ def _draw_tp(k: int):
     widx = int(rng.choice([-1] + free + ([] if group > 1 else list(range(S)))))
     T = int(rng.choice([1, 3, 17, 64, 130]))
     chunk = int(rng.choice([0, 0, 2 * group, 8 * group]))
-    return dict(widths=widths, H=H, S=S, cap=cap, group=group, widx=widx, T=T,
-                delta=bool(rng.integers(0, 2)), norm=bool(rng.integers(0, 2)),
-                gram=bool(rng.integers(0, 2)), pdl=bool(rng.integers(0, 2)),
-                chunk=chunk or None, pad=int(rng.choice([0, 8])))
+    c = dict(widths=widths, H=H, S=S, cap=cap, group=group, widx=widx, T=T,
+             delta=bool(rng.integers(0, 2)), norm=bool(rng.integers(0, 2)),
+             gram=bool(rng.integers(0, 2)), pdl=bool(rng.integers(0, 2)),
+             chunk=chunk or None, pad=int(rng.choice([0, 8])))
+    c["form"] = _draw_form(rng, widths, S, c["delta"])
+    return c
+
+
+def _draw_form(rng, widths, S, delta):
+    """Automatic, one CTA per row, or the ring at a depth every shard fits."""
+    k = int(rng.integers(0, 4))
+    if k == 0:
+        return {}
+    if k == 1:
+        return dict(kernel=ar.KERNEL_GENERIC)
+    fit = [st for st in (2, 3, 4) if ring_fits(max(widths), S, delta, True, st)]
+    if not fit:
+        return dict(kernel=ar.KERNEL_GENERIC)
+    return dict(kernel=ar.KERNEL_STREAM, stages=int(rng.choice(fit)))
 
 
 @pytest.mark.parametrize("k", range(24))
@@ -256,4 +317,5 @@ def test_random_sharding(k):
     wl = W.make_workload(c["T"], c["S"], capacity=c["cap"], has_delta=c["delta"],
                          has_out_norm=c["norm"], block_write_idx=c["widx"], seed=31_000 + k,
                          H=c["H"], mixing=True, slot_stride=c["H"] + c["pad"], group=c["group"])
-    tp_check(wl, c["widths"], f"tp_random_{c}", gram=c["gram"], pdl=c["pdl"], chunk=c["chunk"])
+    tp_check(wl, c["widths"], f"tp_random_{c}", gram=c["gram"], pdl=c["pdl"], chunk=c["chunk"],
+             **c["form"])
