@@ -214,11 +214,22 @@ attn_res_status_t attn_res_h(int64_t H, attn_res_bf16_t* prefix,
  * memory owned by the caller, 4-byte aligned; sums has sums_row >=
  * attn_res_tp_sums_width(num_blocks, gram) floats between token rows:
  * entries 0..N-1 are sum(x_i^2), N..2N-1 are <x_i, q> over the shard
- * (x_S = c).  layout->flags accepts ATTN_RES_FLAG_PDL and
- * ATTN_RES_FLAG_TP_GRAM only.  One CTA of 32..256 threads per token row.
- * Errors as for attn_res (nothing is launched unless ATTN_RES_OK is
- * returned); a written float buffer that overlaps any other argument is
- * ATTN_RES_EALIAS.
+ * (x_S = c).  layout->flags accepts ATTN_RES_FLAG_PDL, ATTN_RES_FLAG_TP_GRAM,
+ * ATTN_RES_FLAG_KERNEL and ATTN_RES_FLAG_STAGES.  Two kernel forms, the same
+ * results up to fp32 summation order:
+ *   ring (ATTN_RES_KERNEL_STREAM) -- persistent CTAs (as many as fit on the
+ *     device, at most T) each streaming every G-th token row's rows through
+ *     a shared-memory ring filled by bulk copies (TMA), ATTN_RES_FLAG_STAGES
+ *     2..4 deep (default 2); the Gram sums on warp-level tensor-core tiles;
+ *   one CTA of 32..256 threads per token row (ATTN_RES_KERNEL_GENERIC).
+ * Automatic: the ring from 1024 token rows when it fits in 220 KB of shared
+ * memory (2 stages of num_blocks + 1 (+1 with delta) rows of Hs columns, plus
+ * 4*Hs bytes and the warps' tiles for the Gram sums), else one CTA per row.
+ * A forced ring that does not fit, another KERNEL value, or STAGES with
+ * ATTN_RES_KERNEL_GENERIC is ATTN_RES_EINVAL; with the automatic form
+ * STAGES applies only when the ring runs.  Errors as for attn_res (nothing
+ * is launched unless ATTN_RES_OK is returned); a written float buffer that
+ * overlaps any other argument is ATTN_RES_EALIAS.
  *
  * Single exchange (ATTN_RES_FLAG_TP_GRAM set on attn_res_tp_sums and
  * attn_res_tp_finish): attn_res_tp_sums also writes g_ij = <x_i, x_j> over
