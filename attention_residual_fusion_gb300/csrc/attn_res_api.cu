@@ -358,6 +358,7 @@ attn_res_status_t check_rows(const RowArgs& a, Params* p) {
   p->bank_group = group;
   p->tokens = T;
   p->inv_h = 1.0f / static_cast<float>(H);
+  p->width = H;
   p->err = nullptr;
   return ATTN_RES_OK;
 }
@@ -395,20 +396,21 @@ attn_res_status_t run(int64_t H, attn_res_bf16_t* prefix, const attn_res_bf16_t*
   if (make_plan(T, num_blocks, out_norm_w != nullptr, layout->flags, bank_group(layout) > 1,
                 &plan) != ATTN_RES_OK)
     return ATTN_RES_EINVAL;
-  // other widths, when H is a multiple of 1024 and the CTAs of a row
-  // exchange sums: the any-width forms -- the split kernel below 80 tokens
-  // (up to 8 CTAs per row), else the stream kernel (up to 16); otherwise the
-  // general kernel; no shape overrides
+  // other widths up to 16384 whose CTAs of a row exchange sums: the
+  // any-width forms, ceil(H / 1024) CTAs per row (the last one owning the
+  // remainder) -- the split kernel below 80 tokens (up to 8 CTAs per row),
+  // else the stream kernel (up to 16); otherwise the general kernel; no
+  // shape overrides
   if (H != kH) {
     const uint32_t f = layout->flags;
     const int forced = static_cast<int>((f >> 16) & 0xfu);
     const bool overrides = ((f >> 8) & 0xffu) != 0 || ((f >> 20) & 0xffu) != 0;
-    const bool any_width = H % attn_res_dev::kRtCols == 0 &&
-                           H / attn_res_dev::kRtCols <= attn_res_dev::kRtMaxK;
+    const int64_t kcols = (H + attn_res_dev::kRtCols - 1) / attn_res_dev::kRtCols;
+    const bool any_width = kcols <= attn_res_dev::kRtMaxK;
     const bool exchange = num_blocks > 0 || out_norm_w != nullptr;
     if (forced == ATTN_RES_KERNEL_STREAM && (!any_width || overrides || !exchange))
       return ATTN_RES_EINVAL;
-    const int kc = static_cast<int>(H / attn_res_dev::kRtCols);
+    const int kc = static_cast<int>(kcols);
     const bool split_ok = any_width && exchange && kc <= attn_res_dev::kSplitRtMaxK;
     if (forced == ATTN_RES_KERNEL_SPLIT && (!split_ok || overrides)) return ATTN_RES_EINVAL;
     const bool auto_fast = forced == 0 && !overrides && any_width && exchange;

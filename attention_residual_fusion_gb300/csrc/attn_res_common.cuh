@@ -24,6 +24,7 @@ struct Params {
   int64_t prefix_row, delta_row, blocks_token, blocks_slot, out_row;
   int64_t bank_group;  // B: token rows per bank row (>= 1)
   float inv_h;         // 1 / H (the kernels built for H = 7168 use a constant)
+  int64_t width;       // H (the any-width kernels: the last CTA's slice may be short)
   int64_t tokens;      // T
   int write_idx;
   float eps, out_eps;

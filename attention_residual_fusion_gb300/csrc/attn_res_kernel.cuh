@@ -24,8 +24,9 @@
 
 namespace attn_res_dev {
 
-// K = 0: any width H that is a multiple of 1024 up to 8192 -- H / 1024 CTAs
-// per token row (read from the cluster shape), 1024 columns each.
+// K = 0: any width H (a multiple of 8) up to 8192 -- ceil(H / 1024) CTAs per
+// token row (read from the cluster shape), 1024 columns each, the last CTA
+// the remainder.
 constexpr int kSplitRtMaxK = 8;
 
 template <int S, bool HAS_DELTA, bool HAS_ONORM, int K>
@@ -61,8 +62,9 @@ __global__ void __launch_bounds__(SplitCfg<S, HAS_DELTA, HAS_ONORM, K>::THREADS)
   // Without a cluster the CTAs of a token are ordinary neighbours in x.
   const uint32_t rank = COMM ? cluster_ctarank() : (blockIdx.x % sp.kc);
   const int64_t t = blockIdx.x / sp.kc;
-  const bool active = C::FULL || tid < C::VPC;
   const int64_t col = (int64_t)(rank * C::VPC + tid) * kVec;
+  // the last CTA of an any-width row may own fewer than 1024 columns
+  const bool active = (C::FULL || tid < C::VPC) && (K != 0 || col < p.width);
 
   if (COMM) {
     if (tid == 0) {

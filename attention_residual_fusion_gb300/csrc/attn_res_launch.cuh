@@ -108,13 +108,22 @@ cudaError_t launch_stream(const Params& p, int64_t T, bool pdl, cudaStream_t str
                           int device, int kc) {
   using C = attn_res_dev::StreamCfg<S, D, O, K, VPT, STAGES>;
   void (*kern)(Params, int64_t) = attn_res_dev::attn_res_stream_kernel<S, D, O, K, VPT, STAGES, G>;
-  // CTAs per token row: K, or (K = 0, any width) kc = H / 1024 from the caller
+  // any width not a multiple of 1024: the entry point with a short last slice
+  int ragged = 0;
+  if constexpr (K == 0) {
+    if (p.width % attn_res_dev::kRtCols != 0) {
+      kern = attn_res_dev::attn_res_stream_ragged_kernel<S, D, O, VPT, STAGES, G>;
+      ragged = 1;
+    }
+  }
+  // CTAs per token row: K, or (K = 0, any width) kc = ceil(H / 1024) from the caller
   if (K != 0) kc = K;
   if (device < 0 || device >= 64 || kc < 1 || kc > attn_res_dev::kRtMaxK)
     return cudaErrorInvalidValue;
-  // per device and split: attributes set and the number of co-resident clusters
-  static std::atomic<int> clusters_per_device[64][attn_res_dev::kRtMaxK + 1];
-  int ncl_max = clusters_per_device[device][kc].load(std::memory_order_acquire);
+  // per device, split and entry point: attributes set and the number of
+  // co-resident clusters
+  static std::atomic<int> clusters_per_device[64][attn_res_dev::kRtMaxK + 1][2];
+  int ncl_max = clusters_per_device[device][kc][ragged].load(std::memory_order_acquire);
   if (ncl_max == 0) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)C::SMEM_BYTES);
@@ -146,7 +155,7 @@ cudaError_t launch_stream(const Params& p, int64_t T, bool pdl, cudaStream_t str
       ncl_max = per_sm * sms / kc;
     }
     if (ncl_max < 1) return cudaErrorInvalidConfiguration;
-    clusters_per_device[device][kc].store(ncl_max, std::memory_order_release);
+    clusters_per_device[device][kc][ragged].store(ncl_max, std::memory_order_release);
   }
   const int64_t ncl = T < ncl_max ? T : ncl_max;
   cudaLaunchAttribute attrs[2];

@@ -38,9 +38,10 @@
 
 namespace attn_res_dev {
 
-// K = 0: any width H that is a multiple of kRtCols -- H / kRtCols CTAs per
-// token row (1..kRtMaxK, read at run time from the cluster shape), each
-// owning kRtCols columns; otherwise K CTAs split the 7168 columns.
+// K = 0: any width H (a multiple of 8) up to kRtMaxK * kRtCols --
+// ceil(H / kRtCols) CTAs per token row (read at run time from the cluster
+// shape), each owning kRtCols columns and the last one the remainder;
+// otherwise K CTAs split the 7168 columns.
 constexpr int kRtCols = 1024;
 constexpr int kRtMaxK = 16;
 
@@ -72,11 +73,14 @@ struct StreamCfg {
 };
 
 // GROUPED: B token rows per bank row with B > 1 possible (else B == 1 and the
-// token loop carries no test for it).
-template <int S, bool HAS_DELTA, bool HAS_ONORM, int K, int VPT, int STAGES, bool GROUPED>
-__global__ void __launch_bounds__(StreamCfg<S, HAS_DELTA, HAS_ONORM, K, VPT, STAGES>::THREADS,
-                                  StreamCfg<S, HAS_DELTA, HAS_ONORM, K, VPT, STAGES>::MIN_BLOCKS)
-    attn_res_stream_kernel(const Params p, const int64_t T) {
+// token loop carries no test for it).  RAGGED (K = 0 only): the last CTA of a
+// row may own fewer than kRtCols columns (H not a multiple of kRtCols); its
+// loads and stores past H are predicated off, its bank-row copies shortened,
+// and the tail of its stage slots zeroed.  Without RAGGED every vector of a
+// slice is in the row, as the tuned shapes need.
+template <int S, bool HAS_DELTA, bool HAS_ONORM, int K, int VPT, int STAGES, bool GROUPED, bool RAGGED>
+__device__ __forceinline__ void stream_body(const Params& p, const int64_t T) {
+  static_assert(K == 0 || !RAGGED, "only the any-width form has a short last slice");
   using C = StreamCfg<S, HAS_DELTA, HAS_ONORM, K, VPT, STAGES>;
   using Tok = typename C::Tok;
   constexpr int VPC = C::VPC;
@@ -105,9 +109,16 @@ __global__ void __launch_bounds__(StreamCfg<S, HAS_DELTA, HAS_ONORM, K, VPT, STA
   int64_t col[VPT];
 #pragma unroll
   for (int v = 0; v < VPT; ++v) {
-    active[v] = ((v + 1) * THREADS <= VPC) || (tid + v * THREADS < VPC);
     col[v] = slice0 + (int64_t)(tid + v * THREADS) * kVec;
+    active[v] = (((v + 1) * THREADS <= VPC) || (tid + v * THREADS < VPC)) &&
+                (!RAGGED || col[v] < p.width);
   }
+  // bytes of one row's slice of this CTA: fixed, or (ragged) what is left of
+  // the row, a multiple of 16
+  const uint32_t slice_bytes =
+      !RAGGED ? C::SLICE_BYTES
+              : (uint32_t)((p.width - slice0 < (int64_t)VPC * kVec ? p.width - slice0
+                                                                  : (int64_t)VPC * kVec) * 2);
 
   if (tid == 0) {
 #pragma unroll
@@ -117,6 +128,14 @@ __global__ void __launch_bounds__(StreamCfg<S, HAS_DELTA, HAS_ONORM, K, VPT, STA
     }
     if (COMM) mailbox_init(mb);
     fence_mbar_init();
+  }
+  // ragged: the stage slots are read in full without a predicate; past a
+  // short last slice (which the copies do not reach) they hold zeros, so the
+  // sums and the mix see zero columns there
+  if (RAGGED && slice_bytes < C::SLICE_BYTES) {
+    const int tail = (int)(C::SLICE_BYTES - slice_bytes) / 16;
+    for (int e = tid; e < STAGES * S * tail; e += THREADS)
+      ring[(e / tail) * VPC + (int)(slice_bytes / 16) + e % tail] = make_uint4(0, 0, 0, 0);
   }
   if (COMM) {
     cluster_arrive_release();  // matched by the wait before the first remote store
@@ -130,12 +149,12 @@ __global__ void __launch_bounds__(StreamCfg<S, HAS_DELTA, HAS_ONORM, K, VPT, STA
   // instruction
   auto issue_bank = [&](int64_t t, int s) {
     const uint32_t bar = smem_addr(&full_bar[s]);
-    if (lane == 0) mbar_arrive_expect_tx(bar, C::STAGE_BYTES);
+    if (lane == 0) mbar_arrive_expect_tx(bar, RAGGED ? S * slice_bytes : C::STAGE_BYTES);
     __syncwarp();
     if (lane < S)
       bulk_load(ring_addr + (uint32_t)(s * S + lane) * C::SLICE_BYTES,
                 bank_of<GROUPED>(p, t) + slice0 + (int64_t)lane * p.blocks_slot,
-                C::SLICE_BYTES, bar);
+                RAGGED ? slice_bytes : C::SLICE_BYTES, bar);
   };
   // every thread: its vectors of the token's prefix and delta rows
   auto load_current = [&](int64_t t, uint4 (&pre)[VPT], uint4 (&del)[VPT]) {
@@ -198,7 +217,7 @@ __global__ void __launch_bounds__(StreamCfg<S, HAS_DELTA, HAS_ONORM, K, VPT, STA
     if (tid == 0 && !was_failed && !failed) pending &= ~(1u << s);
     const uint4* stage = stage_of(j);
     token_sums<S, HAS_DELTA, HAS_ONORM, (K ? K : kRtMaxK), NW, VPT>(
-        [&](int i, int v) { return active[v] ? stage[i * VPC + v * THREADS] : make_uint4(0, 0, 0, 0); },
+        [&](int i, int v) { return (RAGGED || active[v]) ? stage[i * VPC + v * THREADS] : make_uint4(0, 0, 0, 0); },
         cc, q, mb, b, rank, warp, lane, sp);
   };
 
@@ -215,7 +234,7 @@ __global__ void __launch_bounds__(StreamCfg<S, HAS_DELTA, HAS_ONORM, K, VPT, STA
     // B(j): softmax and mix; each warp releases the stage after its last read
     f32x2 acc[VPT][4];
     token_mix<S, HAS_DELTA, HAS_ONORM, (K ? K : kRtMaxK), NW, VPT>(
-        [&](int i, int v) { return active[v] ? stage[i * VPC + v * THREADS] : make_uint4(0, 0, 0, 0); },
+        [&](int i, int v) { return (RAGGED || active[v]) ? stage[i * VPC + v * THREADS] : make_uint4(0, 0, 0, 0); },
         mb, b, bparity, rank, warp, lane, p.eps, failed, p.err,
         [&]() {
           __syncwarp();
@@ -277,6 +296,21 @@ __global__ void __launch_bounds__(StreamCfg<S, HAS_DELTA, HAS_ONORM, K, VPT, STA
       if (pending & (1u << s))
         (void)mbar_wait_bounded(smem_addr(&full_bar[s]), (pending_parity >> s) & 1u);
   }
+}
+
+template <int S, bool HAS_DELTA, bool HAS_ONORM, int K, int VPT, int STAGES, bool GROUPED>
+__global__ void __launch_bounds__(StreamCfg<S, HAS_DELTA, HAS_ONORM, K, VPT, STAGES>::THREADS,
+                                  StreamCfg<S, HAS_DELTA, HAS_ONORM, K, VPT, STAGES>::MIN_BLOCKS)
+    attn_res_stream_kernel(const Params p, const int64_t T) {
+  stream_body<S, HAS_DELTA, HAS_ONORM, K, VPT, STAGES, GROUPED, false>(p, T);
+}
+
+// Any width H that is not a multiple of kRtCols (the last CTA's slice short).
+template <int S, bool HAS_DELTA, bool HAS_ONORM, int VPT, int STAGES, bool GROUPED>
+__global__ void __launch_bounds__(StreamCfg<S, HAS_DELTA, HAS_ONORM, 0, VPT, STAGES>::THREADS,
+                                  StreamCfg<S, HAS_DELTA, HAS_ONORM, 0, VPT, STAGES>::MIN_BLOCKS)
+    attn_res_stream_ragged_kernel(const Params p, const int64_t T) {
+  stream_body<S, HAS_DELTA, HAS_ONORM, 0, VPT, STAGES, GROUPED, true>(p, T);
 }
 
 }  // namespace attn_res_dev

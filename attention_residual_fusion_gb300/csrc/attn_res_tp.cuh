@@ -116,6 +116,23 @@ __device__ __forceinline__ void cta_sum(const float (&v)[NR], float (*scratch)[N
   __syncthreads();
 }
 
+// Sum NR per-thread values over the CTA with one barrier: the warps' totals
+// go to scratch, and thread r (r < NR, then r + blockDim.x, ...) adds column
+// r over the warps in warp order and hands it to store(r, total).  scratch
+// must not be written again before every thread has passed a later barrier
+// (double-buffer it across tokens).
+template <int NR, class Store>
+__device__ __forceinline__ void cta_sum_store(const float (&v)[NR], float (*scratch)[NR], Store store) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  warp_groups<NR, 0>(v, scratch, warp, lane);
+  __syncthreads();
+  for (int r = threadIdx.x; r < NR; r += blockDim.x) {
+    float s = scratch[0][r];
+    for (int w = 1; w < nw; ++w) s += scratch[w][r];
+    store(r, s);
+  }
+}
+
 template <bool HAS_DELTA>
 __device__ __forceinline__ uint4 tp_current(const Params& p, int64_t t, int64_t col) {
   const uint4 pv = ld_row(p.prefix + t * p.prefix_row + col);
@@ -538,6 +555,15 @@ __global__ void __launch_bounds__(TpRingCfg<S, HAS_DELTA, PHASE, HAS_ONORM, GRAM
     const int b = (int)(j & 1);
     float next[2] = {0.f, 0.f};  // reduced input of the next token, in flight meanwhile
     if (NS > 0 && j + 1 < ntok) load_reduced(j + 1, next);
+    // the weights (and the output norm's scale) need only the reduced sums:
+    // take them while the token's rows are still arriving
+    float w[N];
+    float ro = 1.f;
+    if constexpr (PHASE != 0) {
+      tp_weights<S>(sv[b], a.inv_h, p.eps, w);
+      if constexpr (PHASE == 2 && HAS_ONORM)
+        ro = rsqrtf(fmaf(GRAM ? tp_gram_sq<S>(sv[b], w) : sv[b][NR], a.inv_h, p.out_eps));
+    }
     const bool was_failed = failed;
     wait_or_flag(smem_addr(&full_bar[s]), parity, failed, p.err, kErrStageTimeout);
     if (tid == 0 && !was_failed && !failed) pending &= ~(1u << s);
@@ -559,8 +585,7 @@ __global__ void __launch_bounds__(TpRingCfg<S, HAS_DELTA, PHASE, HAS_ONORM, GRAM
         tp_accumulate<S, false>(x, q, ss, dt, part);
       }
       tp_fold<S, false>(ss, dt, part);
-      cta_sum<NT>(part, scratch[b]);
-      for (int r = tid; r < NT; r += nthr) a.sums[t * a.sums_row + r] = scratch[b][0][r];
+      cta_sum_store<NT>(part, scratch[b], [&](int r, float v) { a.sums[t * a.sums_row + r] = v; });
     } else if constexpr (MMA) {
       // c into the stage's prefix row, so that rows 0..S are the sources
       if constexpr (HAS_DELTA) {
@@ -629,8 +654,6 @@ __global__ void __launch_bounds__(TpRingCfg<S, HAS_DELTA, PHASE, HAS_ONORM, GRAM
         a.sums[t * a.sums_row + r] = v1;
       }
     } else {
-      float w[N];
-      tp_weights<S>(sv[b], a.inv_h, p.eps, w);
       if constexpr (PHASE == 1) {
         f32x2 sq2 = 0ull;
         for (int64_t v = tid; v < nv; v += nthr) {
@@ -641,12 +664,8 @@ __global__ void __launch_bounds__(TpRingCfg<S, HAS_DELTA, PHASE, HAS_ONORM, GRAM
         }
         store_reduced(sv[b ^ 1], next);
         const float sq[1] = {f2_lo(sq2) + f2_hi(sq2)};
-        cta_sum<1>(sq, scratch[b]);
-        if (tid == 0) a.sq[t] = scratch[b][0][0];
+        cta_sum_store<1>(sq, scratch[b], [&](int, float v) { a.sq[t] = v; });
       } else {
-        float ro = 1.f;
-        if constexpr (HAS_ONORM)
-          ro = rsqrtf(fmaf(GRAM ? tp_gram_sq<S>(sv[b], w) : sv[b][NR], a.inv_h, p.out_eps));
         const bool slot_write = writes_slot(p, t);
         uint16_t* const slot = slot_write ? const_cast<uint16_t*>(bank_of(p, t)) +
                                                 (int64_t)p.write_idx * p.blocks_slot

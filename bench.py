@@ -72,7 +72,7 @@ def make(name: str):
     if kind == "decode":           # decode:T
         T = int(a[0])
         return W.decode_batch(T), f"decode batch T={T}, S=8, delta, output norm, per-block scales U(0.5,20)"
-    if kind == "width":            # width:H:T:S -- another model width (general kernel)
+    if kind == "width":            # width:H:T:S -- another model width (attn_res_h)
         H, T, S = (int(x) for x in a)
         return (W.make_workload(T, S, capacity=8, has_delta=True, has_out_norm=True,
                                 block_write_idx=7, seed=0, outliers=True, H=H,
@@ -337,17 +337,18 @@ def sweep_prefill(ar, torch, dev, stream, peak):
     return rows
 
 
-WIDTHS = ["width:4096:2048:8", "width:8192:2048:8"]
+WIDTHS = ["width:4096:2048:8", "width:8192:2048:8", "width:3000:2048:8"]
 
 
 def width_kernel(wl) -> str:
     """Kernel attn_res_h runs for the workload's width (the routing its
-    header documents): multiples of 1024 with a row exchange take the
-    any-width split (T < 80) or stream form, every other width the general
-    kernel."""
+    header documents): widths up to 16384 with a row exchange take the
+    any-width split (T < 80, up to 8 CTAs) or stream form with ceil(H / 1024)
+    CTAs per row, every other row the general kernel."""
     exchange = wl.num_blocks > 0 or wl.out_norm_w is not None
-    if wl.H % 1024 == 0 and exchange and wl.H // 1024 <= 16:
-        return "any-width split" if wl.T < 80 and wl.H // 1024 <= 8 else "any-width stream"
+    kc = -(-wl.H // 1024)
+    if exchange and kc <= 16:
+        return "any-width split" if wl.T < 80 and kc <= 8 else "any-width stream"
     return "general"
 
 

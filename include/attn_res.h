@@ -171,14 +171,16 @@ attn_res_status_t attn_res(attn_res_bf16_t* prefix, const attn_res_bf16_t* delta
  * multiple of 8 (one 16-byte vector); every [H]- and row-sized argument above
  * is then H elements wide and strides must be >= H.  H == ATTN_RES_HIDDEN
  * behaves exactly like attn_res.  Other widths:
- *   - H a multiple of 1024, at most 16384, with bank rows or an output norm:
- *     any-width forms of the fast kernels with H / 1024 CTAs per token row
- *     (one cluster) of 1024 columns each -- below 80 token rows and up to
- *     H = 8192 the split kernel (one vector per thread), else the stream
- *     kernel (the per-CTA layout of the (7,2,2) shape); KERNEL(SPLIT) or
- *     KERNEL(STREAM) force one of them; shape overrides are ATTN_RES_EINVAL;
- *   - otherwise a general kernel (one CTA of 256 threads per token row, same
- *     fp32 arithmetic, the rows read three times through L2), a functional
+ *   - H at most 16384, with bank rows or an output norm: any-width forms of
+ *     the fast kernels with ceil(H / 1024) CTAs per token row (one cluster)
+ *     of 1024 columns each, the last CTA owning the remainder -- below 80
+ *     token rows and up to H = 8192 the split kernel (one vector per
+ *     thread), else the stream kernel (the per-CTA layout of the (7,2,2)
+ *     shape); KERNEL(SPLIT) or KERNEL(STREAM) force one of them; shape
+ *     overrides are ATTN_RES_EINVAL;
+ *   - otherwise (wider rows, or neither bank rows nor an output norm) a
+ *     general kernel (one CTA of 256 threads per token row, same fp32
+ *     arithmetic, the rows read three times through L2), a functional
  *     path.  ATTN_RES_FLAG_KERNEL(ATTN_RES_KERNEL_GENERIC) forces it, also at
  *     H == ATTN_RES_HIDDEN.  Forcing a fast kernel where no form of it fits
  *     the width (or the row has no exchange) is ATTN_RES_EINVAL.

@@ -209,25 +209,26 @@ def test_other_widths_validate_strides(lib):
     kw["layout"].prefix_row = 56
     assert ar.call_raw(**kw, H=64) == 1             # stride below H
     kw = good_h(64)
-    kw["layout"].flags = ar.FLAG_KERNEL(2)
-    assert ar.call_raw(**kw, H=64) == 1             # the stream kernel wants H a multiple of 1024
-    kw["layout"].flags = ar.FLAG_KERNEL(1)
-    assert ar.call_raw(**kw, H=64) == 1             # the split kernel is built for 7168 only
+    kw["layout"].flags = ar.FLAG_KERNEL(2) | ar.FLAG_VPT(4)
+    assert ar.call_raw(**kw, H=64) == 1             # no shape overrides at other widths
+    kw["layout"].flags = ar.FLAG_KERNEL(1) | ar.FLAG_SPLIT(7)
+    assert ar.call_raw(**kw, H=64) == 1
 
 
 def test_any_width_stream_checks(lib):
-    """Multiples of 1024 up to 16384 may take the stream kernel's any-width
-    form, in its one shape; other widths and shape overrides may not."""
+    """Widths up to 16384 may take the stream kernel's any-width form
+    (ceil(H / 1024) CTAs per row), in its one shape; wider rows and shape
+    overrides may not."""
     import torch
     no_gpu = not torch.cuda.is_available()
-    for Hh in (1024, 4096, 16384):
+    for Hh in (64, 1000, 1024, 1536, 4000, 4096, 16376, 16384):
         kw = good_h(Hh, T=200)
         kw["layout"].flags = ar.FLAG_KERNEL(2)
         if no_gpu:
             assert ar.call_raw(**kw, H=Hh) in (4, 5)
         kw["layout"].flags = ar.FLAG_KERNEL(2) | ar.FLAG_VPT(2)
         assert ar.call_raw(**kw, H=Hh) == 1
-    for Hh in (17408, 4000, 1536):                   # 17 CTAs; not a multiple of 1024
+    for Hh in (17408, 16392):                        # 17 CTAs per row
         kw = good_h(Hh, T=200)
         kw["layout"].flags = ar.FLAG_KERNEL(2)
         assert ar.call_raw(**kw, H=Hh) == 1
@@ -245,9 +246,15 @@ def test_any_width_stream_checks(lib):
         assert ar.call_raw(**kw, H=8192) in (4, 5)
     kw["layout"].flags = ar.FLAG_KERNEL(1) | ar.FLAG_SPLIT(8)
     assert ar.call_raw(**kw, H=8192) == 1           # no overrides
-    kw = good_h(9216, T=4)
-    kw["layout"].flags = ar.FLAG_KERNEL(1)
-    assert ar.call_raw(**kw, H=9216) == 1           # 9 CTAs per row
+    for Hh in (9216, 8200):                          # 9 CTAs per row
+        kw = good_h(Hh, T=4)
+        kw["layout"].flags = ar.FLAG_KERNEL(1)
+        assert ar.call_raw(**kw, H=Hh) == 1
+    for Hh in (8, 1000, 8184):                       # 1 .. 8 CTAs, a short last one
+        kw = good_h(Hh, T=4)
+        kw["layout"].flags = ar.FLAG_KERNEL(1)
+        if no_gpu:
+            assert ar.call_raw(**kw, H=Hh) in (4, 5)
 
 
 # ---- hidden-sharded entry points (host checks only) ----

@@ -293,7 +293,8 @@ def test_generic_width_against_oracle(H, S):
     wl = W.make_workload(37, S, capacity=9, has_delta=bool(i & 1), has_out_norm=bool(i & 2),
                          block_write_idx=[-1, S, 8][i % 3], seed=i, H=H, mixing=True,
                          slot_stride=H + 8 * (i % 2))
-    full_check(wl, tag=f"generic_H{H}_S{S}")
+    full_check(wl, tag=f"generic_H{H}_S{S}", kernel=ar.KERNEL_GENERIC)
+    full_check(wl, tag=f"auto_H{H}_S{S}")
 
 
 @pytest.mark.parametrize("S", [0, 4, 8])
@@ -387,6 +388,31 @@ def test_any_width_stream_forced_small_T_and_groups(H):
                          block_write_idx=7, seed=H + 1, H=H, mixing=True, group=3)
     full_check(wl, tag=f"anywidth_group_H{H}")
 
+
+
+# ---- any-width forms at widths that are not multiples of 1024 ----------------------
+
+RAGGED = [(H, S) for H in (8, 200, 1000, 1032, 3000, 7000, 8200, 15000, 16376) for S in (0, 4, 8)]
+
+
+@pytest.mark.parametrize("H,S", RAGGED, ids=[f"H{H}_S{S}" for H, S in RAGGED])
+def test_ragged_width_fast_kernels(H, S):
+    """ceil(H / 1024) CTAs per token row, the last one owning the remainder
+    (8 .. 1016 columns; its bank-row copies are that short): the stream form
+    at 131 rows (forced and automatic), the split form at 5 rows (up to 8
+    CTAs); delta, write-back and padded slots varying by case."""
+    i = H + S
+    kc = -(-H // 1024)
+    wl = W.make_workload(131, S, capacity=9, has_delta=bool(i & 1), has_out_norm=True,
+                         block_write_idx=[-1, S, 8][i % 3], seed=7000 + i, H=H, mixing=True,
+                         slot_stride=H + 8 * (i % 2), outliers=bool(i & 2))
+    full_check(wl, tag=f"ragged_stream_H{H}_S{S}", kernel=ar.KERNEL_STREAM)
+    full_check(wl, tag=f"ragged_auto_H{H}_S{S}")
+    wl = W.make_workload(5, S, capacity=9, has_delta=not (i & 1), has_out_norm=bool(S % 2) or S == 0,
+                         block_write_idx=[8, -1, S][i % 3], seed=7100 + i, H=H, mixing=True)
+    full_check(wl, tag=f"ragged_small_auto_H{H}_S{S}")
+    if kc <= 8:
+        full_check(wl, tag=f"ragged_split_H{H}_S{S}", kernel=ar.KERNEL_SPLIT)
 
 
 SMALLW = [(H, T, S) for H in (1024, 3072, 8192, 12288) for T in (1, 5, 79) for S in (1, 8)]

@@ -1,7 +1,7 @@
 """Seeded random configurations against the oracle.
 
 Each case draws a hidden size (7168, another multiple of 1024, or any
-multiple of 8), a token count, num_blocks, the bank capacity and its padded
+multiple of 8: the any-width forms take every width up to 16384), a token count, num_blocks, the bank capacity and its padded
 slot stride, delta / output norm / write-back, shared bank rows, PDL, and a
 kernel (automatic or forced where the width allows it), then checks the CUDA
 path against the oracle with the bar of the other parity tests: out within
@@ -47,8 +47,10 @@ def draw(k: int):
     kernels = [0]
     if H == 7168:
         kernels += [ar.KERNEL_SPLIT, ar.KERNEL_STREAM, ar.KERNEL_GENERIC]
-    elif H % 1024 == 0 and (S > 0 or has_norm):
+    elif H <= 16384 and (S > 0 or has_norm):
         kernels += [ar.KERNEL_STREAM, ar.KERNEL_GENERIC]
+        if H <= 8192:
+            kernels += [ar.KERNEL_SPLIT]
     else:
         kernels += [ar.KERNEL_GENERIC]
     kernel = int(rng.choice(kernels))
