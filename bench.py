@@ -279,11 +279,12 @@ def time_device(ar, wl, t, torch, stream, steps, warmup):
     return ev[0].elapsed_time(ev[steps]), per
 
 
-def input_sets(wl, t, torch, dev):
+def input_sets(wl, t, torch, dev, at_least=1):
     """The device inputs plus extra copies, so that cycling through them
-    touches at least 3x the L2 size: every launch then reads from HBM."""
+    touches at least 3x the L2 size: every launch then reads from HBM (and
+    at least `at_least` sets)."""
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    n = min(16, max(1, -(-3 * l2 // wl.algorithmic_bytes())))
+    n = min(16, max(at_least, -(-3 * l2 // wl.algorithmic_bytes())))
     sets = [t]
     for _ in range(n - 1):
         sets.append({k: (v.clone() if v is not None and k in ("prefix", "delta", "bank", "out") else v)
@@ -291,16 +292,17 @@ def input_sets(wl, t, torch, dev):
     return sets
 
 
-def time_graph(ar, wl, sets, torch, stream, calls=64):
+def time_graph(ar, wl, sets, torch, stream, calls=64, pdl=False):
     """Mean µs per call of `calls` back-to-back launches replayed from a CUDA
-    graph (no host launch overhead), cycling through the input sets."""
+    graph (no host launch overhead), cycling through the input sets; with
+    `pdl` each launch may start while the previous one finishes."""
     for st in sets:
-        call(ar, wl, st, stream)
+        call(ar, wl, st, stream, pdl=pdl)
     torch.cuda.synchronize()
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=stream):
         for i in range(calls):
-            call(ar, wl, sets[i % len(sets)], stream)
+            call(ar, wl, sets[i % len(sets)], stream, pdl=pdl)
     g.replay()
     torch.cuda.synchronize()
     a = torch.cuda.Event(enable_timing=True)
@@ -314,23 +316,30 @@ def time_graph(ar, wl, sets, torch, stream, calls=64):
     return a.elapsed_time(b) * 1e3 / calls
 
 
-SWEEP = ["prefill:1024:0:1:7", "prefill:1024:4:1:7", "prefill:1024:8:1:7",
-         "prefill:2048:0:1:7", "prefill:2048:4:1:7", "prefill:2048:8:1:7"]
+# every prefill case of the benchmark set: T x num_blocks x output norm x write-back
+SWEEP = [f"prefill:{T}:{S}:{o}:{w}" for T in (1024, 2048) for S in (0, 4, 8) for o in (1, 0)
+         for w in (7, -1)]
 
 
 def sweep_prefill(ar, torch, dev, stream, peak):
-    """The other T >= 1024 cells (prefill workloads): µs per call from graph
-    replay over rotating input sets larger than 3x L2."""
+    """The other T >= 1024 cells (every prefill case: T, num_blocks, output
+    norm, write-back): µs per call from graph replay over rotating input sets
+    larger than 3x L2, without and with programmatic dependent launch
+    (`pdl_*`: each call may start while the previous one drains; the input
+    sets rotate, so no call reads rows the previous one writes)."""
     rows = []
     for name in SWEEP:
         wl, _ = make(name)
         t = device_tensors(wl, torch, dev)
-        sets = input_sets(wl, t, torch, dev)
+        sets = input_sets(wl, t, torch, dev, at_least=2)
         us = time_graph(ar, wl, sets, torch, stream)
+        us_pdl = time_graph(ar, wl, sets, torch, stream, pdl=True)
         gbs = wl.algorithmic_bytes() / (us * 1e-6) / 1e9
         rows.append({"workload": name, "us_per_call": round(us, 2),
                      "tokens_per_s": round(wl.T / (us * 1e-6), 1),
                      "gbs": round(gbs, 1), "frac": round(gbs / peak, 4),
+                     "pdl_us_per_call": round(us_pdl, 2),
+                     "pdl_frac": round(wl.algorithmic_bytes() / (us_pdl * 1e-6) / 1e9 / peak, 4),
                      "input_sets": len(sets)})
         del t, sets
         torch.cuda.empty_cache()
