@@ -22,18 +22,19 @@
 // sum_i w_i |x_i|).
 //
 // H in the logits and the norm is the full width, passed in as 1/H.  The
-// per-element arithmetic is that of the other kernels.  One CTA per token
-// row, 32..256 threads (enough to give each thread one 16-byte vector of the
-// shard where it fits).  The mix is recomputed in tp_finish rather than kept
-// between calls, so the only data between calls are the floats per token the
-// caller reduces.
+// per-element arithmetic is that of the other kernels.  Two forms of each
+// phase: one CTA per token row, 32..256 threads (enough to give each thread
+// one 16-byte vector of the shard where it fits), and a persistent ring form
+// (below) for many token rows.  The mix is recomputed in tp_finish rather
+// than kept between calls, so the only data between calls are the floats per
+// token the caller reduces.
 #pragma once
 
 #include "attn_res_common.cuh"
 
 namespace attn_res_dev {
 
-// Warp-level tensor-core tiles (the sums phase of the ring form).
+// Warp-level tensor-core tiles (the Gram sums of the ring form).
 
 // Four 8x8 b16 matrices from shared memory: lane l gives the address of row
 // l % 8 of matrix l / 8 (16 bytes each); r[j] is this lane's part of matrix j.
@@ -395,8 +396,15 @@ __global__ void __launch_bounds__(kTpMaxThreads) attn_res_tp_finish_kernel(const
 // from the stage; after the CTA barrier that ends a token (inside the
 // reduction, or an explicit one in the finish phase) warp 0 refills the
 // stage.  The reduced sums a token needs (and sq) are loaded one token ahead
-// into a double-buffered array in shared memory.  Waits are bounded as in the
-// stream kernel.  The arithmetic per element is that of the kernels above.
+// into a double-buffered array in shared memory, and the softmax weights are
+// taken from them while the token's rows are still arriving.  Waits are
+// bounded as in the stream kernel.  The arithmetic per element is that of the
+// kernels above, except that the Gram sums (45 dot products of 9 rows per
+// token at S = 8: a small dense contraction) run on mma.sync tiles: A and B
+// are the stage's rows (plus the query split into two exact bf16 rows), 16
+// columns per step, the warps' 16 x 16 tiles summed in warp order.  (tcgen05
+// wants tiles of at least 64 rows in its core-matrix layout; a token has 9
+// rows, stored row-major.)
 //
 // PHASE 0: sums; 1: sum of squares of the mix; 2: finish.
 
