@@ -74,13 +74,16 @@ attn_res_status_t make_plan(int64_t T, int num_blocks, bool has_onorm, uint32_t 
     const bool no_bank = !grouped && num_blocks == 0;
     if (pl.split == 0) {
       pl.split = 7;
-      if (no_bank && (pl.vpt == 0 || pl.vpt == 4)) pl.split = 2;
+      if (no_bank && (pl.vpt == 0 || pl.vpt == 4 || pl.vpt == 8)) pl.split = 2;
       if (no_bank && pl.vpt == 2) pl.split = 4;
     }
     if (pl.stages == 0) pl.stages = 2;
     if (pl.vpt == 0) {
       const bool one_warp = pl.split == 7 && num_blocks >= 1 && num_blocks <= 5 && has_onorm;
-      pl.vpt = (!grouped && (one_warp || pl.split == 2)) ? 4 : 2;
+      if (!grouped && pl.split == 2)
+        pl.vpt = no_bank ? 8 : 4;  // (2,8,2): measured 2-5 % faster than (2,4,2) without bank rows
+      else
+        pl.vpt = (!grouped && one_warp) ? 4 : 2;
     }
     pl.shape = stream_shape_index(pl.split, pl.vpt, pl.stages, grouped);
     if (pl.shape < 0) return ATTN_RES_EINVAL;

@@ -47,7 +47,7 @@ StreamLaunchFn pick_stream(bool d, bool o) {
 }  // namespace
 
 StreamLaunchFn ATTN_RES_CAT(stream_launcher_s, ATTN_RES_S)(int shape_idx, bool d, bool o) {
-  static_assert(kNumStreamShapes == 10, "update the switch below");
+  static_assert(kNumStreamShapes == 11, "update the switch below");
   switch (shape_idx) {
     case 0: return pick_stream<0>(d, o);
     case 1: return pick_stream<1>(d, o);
@@ -59,6 +59,7 @@ StreamLaunchFn ATTN_RES_CAT(stream_launcher_s, ATTN_RES_S)(int shape_idx, bool d
     case 7: return pick_stream<7>(d, o);
     case 8: return pick_stream<8>(d, o);
     case 9: return pick_stream<9>(d, o);
+    case 10: return pick_stream<10>(d, o);
     default: return nullptr;
   }
 }

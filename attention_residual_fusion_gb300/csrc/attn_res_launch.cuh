@@ -84,8 +84,8 @@ struct StreamShape {
 // rows allowed.
 constexpr StreamShape kStreamShapes[] = {{7, 1, 2, false}, {7, 2, 2, false}, {7, 2, 3, false},
                                          {7, 4, 2, false}, {4, 2, 2, false}, {4, 2, 3, false},
-                                         {2, 4, 2, false}, {14, 2, 2, false}, {7, 2, 2, true},
-                                         {0, 2, 2, true}};
+                                         {2, 4, 2, false}, {14, 2, 2, false}, {2, 8, 2, false},
+                                         {7, 2, 2, true},  {0, 2, 2, true}};
 constexpr int kNumStreamShapes = sizeof(kStreamShapes) / sizeof(kStreamShapes[0]);
 constexpr int kGroupedStreamShape = kNumStreamShapes - 2;
 constexpr int kAnyWidthStreamShape = kNumStreamShapes - 1;

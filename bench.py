@@ -110,7 +110,8 @@ def kernel_label(wl, shape) -> str:
     """The timed kernel as ncu names it (template arguments of the launch)."""
     d, o = int(wl.delta is not None), int(wl.out_norm_w is not None)
     if shape["kernel"] == "stream":
-        vpt = {(7, 32): 4, (7, 64): 2, (7, 128): 1, (4, 128): 2, (14, 32): 2, (14, 64): 1}
+        vpt = {(7, 32): 4, (7, 64): 2, (7, 128): 1, (4, 128): 2, (14, 32): 2, (14, 64): 1,
+               (2, 128): 4, (2, 64): 8}
         v = vpt.get((shape["split"], shape["threads"]), 0)
         return (f"attn_res_stream_kernel<{wl.num_blocks},{d},{o},{shape['split']},{v},"
                 f"{shape['stages']},{int(wl.group > 1)}>")

@@ -80,10 +80,11 @@ typedef enum {
  *   STAGES(n): ring depth of the stream kernel.
  *   VPT(n):    16-byte vectors per thread and row (split kernel: 1).
  * Stream kernel shapes (split, vpt, stages): (7,1,2) (7,2,2) (7,2,3) (7,4,2)
- * (4,2,2) (4,2,3) (2,4,2) (14,2,2).  Unset fields default to: split 2 with
- * no bank rows (4 if VPT 2 is given, 7 for another VPT), else 7; stages 2;
- * VPT 4 with split 2, or with split 7, 1..5 bank rows and an output norm,
- * else 2 -- so (7,4,2), (2,4,2) with no bank rows, and (7,2,2) otherwise.
+ * (4,2,2) (4,2,3) (2,4,2) (14,2,2) (2,8,2).  Unset fields default to:
+ * split 2 with no bank rows (4 if VPT 2 is given, 7 for VPT 1), else 7;
+ * stages 2; VPT 8 with split 2 and no bank rows, 4 with split 2 and bank
+ * rows or with split 7, 1..5 bank rows and an output norm, else 2 -- so
+ * (7,4,2), (2,8,2) with no bank rows, and (7,2,2) otherwise.
  * The kernel defaults to the split kernel below 80 tokens and when there is
  * neither a bank row nor an output norm, else the stream kernel. */
 #define ATTN_RES_FLAG_SPLIT(k) (((uint32_t)(k) & 0xffu) << 8)

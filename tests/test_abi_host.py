@@ -48,13 +48,15 @@ def test_launch_shape(lib):
     assert ls(8192, 8, True) == dict(kernel="stream", split=7, stages=2, threads=64, ctas=0, cluster=7)
     assert ls(8192, 4, True) == dict(kernel="stream", split=7, stages=2, threads=32, ctas=0, cluster=7)
     assert ls(8192, 4, False) == dict(kernel="stream", split=7, stages=2, threads=64, ctas=0, cluster=7)
-    assert ls(8192, 0, True) == dict(kernel="stream", split=2, stages=2, threads=128, ctas=0, cluster=2)
+    assert ls(8192, 0, True) == dict(kernel="stream", split=2, stages=2, threads=64, ctas=0, cluster=2)
+    assert ls(8192, 0, True, ar.FLAG_VPT(4)) == dict(kernel="stream", split=2, stages=2, threads=128, ctas=0, cluster=2)
+    assert ls(8192, 4, True, ar.FLAG_SPLIT(2))["threads"] == 128      # (2,4,2) with bank rows
     assert ls(8192, 0, True, ar.FLAG_VPT(2))["split"] == 4
     assert ls(8192, 0, True, ar.FLAG_VPT(1))["split"] == 7
     assert ls(8192, 0, True, ar.FLAG_VPT(2) | ar.FLAG_STAGES(3))["split"] == 4
     with pytest.raises(ar.AttnResError):
         ls(8192, 0, True, ar.FLAG_STAGES(3))          # (2,4,3) is not built
-    assert ls(9000, 0, True, ar.FLAG_SPLIT(2))["threads"] == 128
+    assert ls(9000, 0, True, ar.FLAG_SPLIT(2))["threads"] == 64
     # no softmax and no output norm: the CTAs of a token never talk
     assert ls(1024, 0, False) == dict(kernel="split", split=7, stages=0, threads=128, ctas=7168, cluster=1)
     assert ls(2, 8, True, ar.FLAG_SPLIT(16)) == dict(kernel="split", split=16, stages=0, threads=64, ctas=32, cluster=16)

@@ -184,7 +184,8 @@ def test_repeated_calls_are_deterministic():
 
 # ---- the persistent stream kernel ------------------------------------------------
 
-SHAPES = [(7, 1, 2), (7, 2, 2), (7, 2, 3), (7, 4, 2), (4, 2, 2), (4, 2, 3), (2, 4, 2), (14, 2, 2)]
+SHAPES = [(7, 1, 2), (7, 2, 2), (7, 2, 3), (7, 4, 2), (4, 2, 2), (4, 2, 3), (2, 4, 2), (14, 2, 2),
+          (2, 8, 2)]
 STREAM = [(S, sh) for S in range(9) for sh in SHAPES]
 
 
