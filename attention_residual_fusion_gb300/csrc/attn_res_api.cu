@@ -46,8 +46,9 @@ struct Plan {
 //    shape (CTAs per token, vectors per thread, stages):
 //      (7,4,2) with 1..5 bank rows and an output norm: one warp per CTA, so
 //              fewer warps share the reduction and exchange work of a token;
-//      (2,4,2) with no bank rows (output norm only): 2 CTAs of 4 warps per
-//              token, so a token's short exchange spans only two CTAs;
+//      (2,8,2) with no bank rows (output norm only): 2 CTAs of 2 warps per
+//              token, so a token's short exchange spans only two CTAs, and
+//              four such CTAs fit an SM;
 //      (7,2,2) otherwise (6..8 bank rows, or no output norm): two warps per
 //              CTA, more warps per SM to cover the longer per-token work.
 //  * with shared bank rows (B > 1) the stream kernel has one shape, (7,2,2).
