@@ -233,6 +233,34 @@ def test_reductions_are_called_in_order():
                        all_reduce=fake_reduce, phases=STANDIN, chunk_tokens=3, blocks_group=2)
 
 
+def test_kernel_form_reaches_every_phase():
+    """kernel / stages are passed to every phase call (and nothing extra is
+    passed when they are left automatic)."""
+    from attention_residual_fusion_gb300 import tp
+
+    calls = []
+
+    def wrap(name, fn):
+        def f(*a, **kw):
+            calls.append((name, kw.get("kernel"), kw.get("stages")))
+            return fn(*a, **kw)
+        return f
+
+    spy = types.SimpleNamespace(sums=wrap("sums", standin_sums), sq=wrap("sq", standin_sq),
+                                finish=wrap("finish", standin_finish))
+    wl = _workload((8, True, True, 8, 64))
+    args = (_tensor(wl.prefix.copy()), _tensor(wl.delta), _tensor(wl.bank.copy()), 8, 8,
+            _tensor(wl.res_w), _tensor(wl.rms_w), _tensor(wl.out_norm_w))
+    tp.attn_res_tp(*args, H=64, all_reduce=lambda t: None, phases=spy, kernel=2, stages=3)
+    assert calls == [("sums", 2, 3), ("sq", 2, 3), ("finish", 2, 3)]
+    calls.clear()
+    tp.attn_res_tp(*args, H=64, all_reduce=lambda t: None, phases=spy)
+    assert calls == [("sums", None, None), ("sq", None, None), ("finish", None, None)]
+    import attention_residual_fusion_gb300 as ar
+    assert tp._flags(True, True, 2, 3) == (ar.FLAG_PDL | ar.FLAG_TP_GRAM | ar.FLAG_KERNEL(2)
+                                           | ar.FLAG_STAGES(3))
+
+
 def test_standins_pin_to_the_oracle_unsharded():
     """The stand-ins themselves, with no sharding, agree with the oracle (so a
     failure above points at the orchestration)."""
