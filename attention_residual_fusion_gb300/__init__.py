@@ -21,6 +21,12 @@ FLAG_TP_GRAM = 0x2
 KERNEL_SPLIT = 1
 KERNEL_STREAM = 2
 KERNEL_GENERIC = 3
+KERNEL_STAGED = 4
+KERNEL_ROW = 5
+KERNEL_ROW_SMEM = 6
+KERNEL_NAMES = {KERNEL_SPLIT: "split", KERNEL_STREAM: "stream", KERNEL_GENERIC: "generic",
+                KERNEL_STAGED: "staged", KERNEL_ROW: "row",
+                KERNEL_ROW_SMEM: "row_smem"}
 
 
 def FLAG_SPLIT(k: int) -> int:
@@ -95,7 +101,7 @@ def lib():
         L.attn_res_launch_shape.restype = ctypes.c_int
         ip = ctypes.POINTER(ctypes.c_int)
         L.attn_res_launch_shape.argtypes = [
-            ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_uint32,
+            ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_uint32,
             ip, ip, ip, ip, ctypes.POINTER(ctypes.c_int64), ip]
         L.attn_res_device_status.restype = ctypes.c_int
         L.attn_res_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint), ctypes.c_int]
@@ -120,18 +126,19 @@ def status_string(status: int) -> str:
     return lib().attn_res_status_string(status).decode()
 
 
-def launch_shape(T: int, num_blocks: int, has_out_norm: bool, flags: int = 0) -> dict:
+def launch_shape(T: int, num_blocks: int, has_out_norm: bool, flags: int = 0,
+                 has_delta: bool = True) -> dict:
     """Launch attn_res would make: kernel, split, stages, threads per CTA,
     CTAs (0 = persistent grid sized to the device) and cluster size."""
     kern, k, st_, th, cl = (ctypes.c_int() for _ in range(5))
     ctas = ctypes.c_int64()
-    st = lib().attn_res_launch_shape(T, num_blocks, int(has_out_norm), flags,
+    st = lib().attn_res_launch_shape(T, num_blocks, int(has_delta), int(has_out_norm), flags,
                                      ctypes.byref(kern), ctypes.byref(k),
                                      ctypes.byref(st_), ctypes.byref(th),
                                      ctypes.byref(ctas), ctypes.byref(cl))
     if st != 0:
         raise AttnResError(st, status_string(st))
-    return dict(kernel={1: "split", 2: "stream", 3: "generic"}[kern.value], split=k.value,
+    return dict(kernel=KERNEL_NAMES[kern.value], split=k.value,
                 stages=st_.value, threads=th.value, ctas=ctas.value, cluster=cl.value)
 
 

@@ -27,21 +27,40 @@ constexpr uint32_t kKnownFlags = ATTN_RES_FLAG_PDL | ATTN_RES_FLAG_SPLIT(0xff) |
 
 // From this many tokens on, the persistent stream kernel is used.
 constexpr int64_t kStreamMinTokens = 80;
+// From this many tokens on, the wider automatic choices below apply (measured
+// at 256 and 1024 tokens; the switch point between them is not tuned).
+constexpr int64_t kManyTokens = 512;
 
 struct Plan {
-  int kernel;  // ATTN_RES_KERNEL_SPLIT or ATTN_RES_KERNEL_STREAM
+  int kernel;  // ATTN_RES_KERNEL_*
   int split;   // CTAs per token row
-  int stages;  // ring depth (stream kernel), 0 otherwise
+  int stages;  // stream kernel: ring depth; staged form: CTAs per SM; 0 otherwise
   int vpt;     // 16-byte vectors per thread and row
   int shape;   // index into the stream kernel's shape table
 };
 
-// Automatic choice (measured on GB300 over the prefill, decode and long
-// prefill workloads):
+// Automatic choice, from sweeps on GB300 of graph-replayed calls over input
+// copies larger than 3x L2 (num_blocks 0..6 x output norm x T = 256, 1024,
+// 2048, 4096, with delta; decode, prefill and long-prefill workloads):
 //  * few tokens (T < 80: split 5.2 µs vs stream 6.0 µs at T = 64, 8.7 vs 7.6
-//    µs at T = 96, 8 bank rows), or no exchange at all (no bank rows and no output
-//    norm): the split kernel, 7 CTAs x 128 threads per token, all threads
-//    active, so a token's latency chain runs on 7 SMs at once;
+//    µs at T = 96, 8 bank rows), or no exchange at all (no bank rows and no
+//    output norm) below 512 tokens: the split kernel, 7 CTAs x 128 threads per
+//    token, all threads active, so a token's latency chain runs on 7 SMs at
+//    once;
+//  * few bank rows: a row kernel, one CTA per token holding the whole row --
+//    no cluster, and the block scheduler spreads the last rows over every SM
+//    (T = 1024, no bank rows, output norm: 12.0 -> 11.1 µs; one bank row,
+//    T = 256: 7.6 -> 6.4 µs), its rows in registers (up to two bank rows;
+//    7 vectors per thread, or 4 where that fits more CTAs per SM) or, for
+//    more rows or more tokens, in shared memory (7 vectors per thread, two
+//    CTAs per SM; 4 bank rows, T = 256: 10.1 -> 9.4 µs; one bank row,
+//    T = 4096: 52.8 -> 47.5 µs);
+//  * with an output norm, 3..5 bank rows and at least 512 tokens: the staged
+//    form of the stream kernel (prefix and delta also in the ring) in the
+//    shape of the tuned register form, (4,4) at 5 CTAs per SM for 3 bank
+//    rows, (7,4) at 7 for 4, (4,4) at 4 for 5 (T = 1024, 4 bank rows:
+//    23.9 -> 23.0 µs); without the norm, 3 bank rows below 512 tokens: (4,4)
+//    at 5;
 //  * otherwise the stream kernel, persistent clusters with a 2-deep TMA ring,
 //    shape (CTAs per token, vectors per thread, stages):
 //      (7,4,2) with 1..5 bank rows and an output norm: one warp per CTA, so
@@ -51,7 +70,54 @@ struct Plan {
 //              four such CTAs fit an SM;
 //      (7,2,2) otherwise (6..8 bank rows, or no output norm): two warps per
 //              CTA, more warps per SM to cover the longer per-token work.
-//  * with shared bank rows (B > 1) the stream kernel has one shape, (7,2,2).
+//  * with shared bank rows (B > 1) the stream kernel has one shape, (7,2,2),
+//    and neither a row kernel nor the staged form is chosen.
+void auto_plan(int64_t T, int S, bool has_onorm, bool grouped, Plan* pl) {
+  const bool exchange = S > 0 || has_onorm;
+  const bool many = T >= kManyTokens;
+  pl->kernel = ATTN_RES_KERNEL_SPLIT;
+  if (T < kStreamMinTokens || grouped) {
+    if (T >= kStreamMinTokens && exchange) pl->kernel = ATTN_RES_KERNEL_STREAM;
+    return;
+  }
+  auto row = [&](int kernel, int vpt) {
+    pl->kernel = kernel;
+    pl->split = 1;
+    pl->vpt = vpt;
+  };
+  auto staged = [&](int k, int ctas_per_sm) {
+    pl->kernel = ATTN_RES_KERNEL_STAGED;
+    pl->split = k;
+    pl->vpt = 4;
+    pl->stages = ctas_per_sm;
+  };
+  constexpr int REG = ATTN_RES_KERNEL_ROW, SMEM = ATTN_RES_KERNEL_ROW_SMEM;
+  if (has_onorm) {
+    switch (S) {
+      case 0: return row(REG, many ? 7 : 4);
+      case 1: return many ? row(SMEM, 7) : row(REG, 4);
+      case 2: return T >= 4096 ? row(SMEM, 7) : row(REG, 7);
+      case 3: return many ? staged(4, 5) : row(SMEM, 7);
+      case 4: return many ? staged(7, 7) : row(SMEM, 7);
+      case 5: return many ? staged(4, 4) : row(SMEM, 7);
+      default: break;
+    }
+  } else if (!many) {
+    switch (S) {
+      case 0: return;  // the split kernel
+      case 1:
+      case 2: return row(REG, 4);
+      case 3: return staged(4, 5);
+      case 4:
+      case 5: return row(SMEM, 7);
+      default: break;
+    }
+  } else if (S <= 1) {
+    return row(REG, 7);
+  }
+  pl->kernel = ATTN_RES_KERNEL_STREAM;
+}
+
 attn_res_status_t make_plan(int64_t T, int num_blocks, bool has_onorm, uint32_t flags, bool grouped,
                             Plan* out) {
   Plan pl;
@@ -61,8 +127,20 @@ attn_res_status_t make_plan(int64_t T, int num_blocks, bool has_onorm, uint32_t 
   pl.vpt = static_cast<int>((flags >> 24) & 0xfu);
   pl.shape = -1;
   if (pl.kernel == 0) {
-    const bool exchange = num_blocks > 0 || has_onorm;
-    pl.kernel = (T >= kStreamMinTokens && exchange) ? ATTN_RES_KERNEL_STREAM : ATTN_RES_KERNEL_SPLIT;
+    // the automatic kernel; shape overrides given with it still apply below
+    Plan a{0, 0, 0, 0, -1};
+    auto_plan(T, num_blocks, has_onorm, grouped, &a);
+    const bool overrides = pl.split != 0 || pl.stages != 0 || pl.vpt != 0;
+    pl.kernel = a.kernel;
+    if (!overrides) {
+      pl.split = a.split;
+      pl.stages = a.stages;
+      pl.vpt = a.vpt;
+    } else if (a.kernel == ATTN_RES_KERNEL_ROW || a.kernel == ATTN_RES_KERNEL_STAGED) {
+      // shape overrides name a split or stream shape: keep their kernel family
+      const bool exchange = num_blocks > 0 || has_onorm;
+      pl.kernel = (T >= kStreamMinTokens && exchange) ? ATTN_RES_KERNEL_STREAM : ATTN_RES_KERNEL_SPLIT;
+    }
   }
   if (pl.kernel == ATTN_RES_KERNEL_SPLIT) {
     if (pl.split == 0) pl.split = 7;
@@ -86,7 +164,28 @@ attn_res_status_t make_plan(int64_t T, int num_blocks, bool has_onorm, uint32_t 
       else
         pl.vpt = (!grouped && one_warp) ? 4 : 2;
     }
-    pl.shape = stream_shape_index(pl.split, pl.vpt, pl.stages, grouped);
+    pl.shape = stream_shape_index(pl.split, pl.vpt, pl.stages, grouped, false);
+    if (pl.shape < 0) return ATTN_RES_EINVAL;
+  } else if (pl.kernel == ATTN_RES_KERNEL_ROW) {
+    if (pl.split == 0) pl.split = 1;
+    if (pl.vpt == 0) pl.vpt = 7;
+    if (pl.split != 1 || pl.stages != 0 || row_vpt_index(pl.vpt) < 0 ||
+        num_blocks > kRowMaxBlocks)
+      return ATTN_RES_EINVAL;
+  } else if (pl.kernel == ATTN_RES_KERNEL_ROW_SMEM) {
+    if (pl.split == 0) pl.split = 1;
+    if (pl.vpt == 0) pl.vpt = 4;
+    if (pl.split != 1 || pl.stages != 0 || row_vpt_index(pl.vpt) < 0 ||
+        num_blocks < kRowSmemMinBlocks || num_blocks > kRowSmemMaxBlocks)
+      return ATTN_RES_EINVAL;
+  } else if (pl.kernel == ATTN_RES_KERNEL_STAGED) {
+    if (grouped) return ATTN_RES_EINVAL;
+    if (pl.split == 0 && pl.vpt == 0 && pl.stages == 0) {
+      pl.split = num_blocks == 4 ? 7 : 4;
+      pl.vpt = 4;
+      pl.stages = num_blocks == 4 ? 7 : (num_blocks == 5 ? 4 : 5);
+    }
+    pl.shape = stream_shape_index(pl.split, pl.vpt, pl.stages, false, true);
     if (pl.shape < 0) return ATTN_RES_EINVAL;
   } else {
     return ATTN_RES_EINVAL;
@@ -167,6 +266,36 @@ attn_res_status_t check_device(int* dev_out) {
     g_device_state[dev].store(st, std::memory_order_release);
   }
   return st == 1 ? ATTN_RES_OK : ATTN_RES_EDEVICE;
+}
+
+RowLaunchFn lookup_row_smem(int S, int vpt_idx, bool d, bool o) {
+  switch (S) {
+    case 0: return row_smem_launcher_s0(vpt_idx, d, o);
+    case 1: return row_smem_launcher_s1(vpt_idx, d, o);
+    case 2: return row_smem_launcher_s2(vpt_idx, d, o);
+    case 3: return row_smem_launcher_s3(vpt_idx, d, o);
+    case 4: return row_smem_launcher_s4(vpt_idx, d, o);
+    case 5: return row_smem_launcher_s5(vpt_idx, d, o);
+    case 6: return row_smem_launcher_s6(vpt_idx, d, o);
+    case 7: return row_smem_launcher_s7(vpt_idx, d, o);
+    case 8: return row_smem_launcher_s8(vpt_idx, d, o);
+    default: return nullptr;
+  }
+}
+
+RowLaunchFn lookup_row(int S, int vpt_idx, bool d, bool o) {
+  switch (S) {
+    case 0: return row_launcher_s0(vpt_idx, d, o);
+    case 1: return row_launcher_s1(vpt_idx, d, o);
+    case 2: return row_launcher_s2(vpt_idx, d, o);
+    case 3: return row_launcher_s3(vpt_idx, d, o);
+    case 4: return row_launcher_s4(vpt_idx, d, o);
+    case 5: return row_launcher_s5(vpt_idx, d, o);
+    case 6: return row_launcher_s6(vpt_idx, d, o);
+    case 7: return row_launcher_s7(vpt_idx, d, o);
+    case 8: return row_launcher_s8(vpt_idx, d, o);
+    default: return nullptr;
+  }
 }
 
 GenericLaunchFn lookup_generic(int S, bool d, bool o) {
@@ -412,7 +541,9 @@ attn_res_status_t run(int64_t H, attn_res_bf16_t* prefix, const attn_res_bf16_t*
     const int64_t kcols = (H + attn_res_dev::kRtCols - 1) / attn_res_dev::kRtCols;
     const bool any_width = kcols <= attn_res_dev::kRtMaxK;
     const bool exchange = num_blocks > 0 || out_norm_w != nullptr;
-    if (forced == ATTN_RES_KERNEL_STREAM && (!any_width || overrides || !exchange))
+    if ((forced == ATTN_RES_KERNEL_STREAM && (!any_width || overrides || !exchange)) ||
+        forced == ATTN_RES_KERNEL_STAGED || forced == ATTN_RES_KERNEL_ROW ||
+        forced == ATTN_RES_KERNEL_ROW_SMEM)
       return ATTN_RES_EINVAL;
     const int kc = static_cast<int>(kcols);
     const bool split_ok = any_width && exchange && kc <= attn_res_dev::kSplitRtMaxK;
@@ -467,6 +598,11 @@ attn_res_status_t run(int64_t H, attn_res_bf16_t* prefix, const attn_res_bf16_t*
       GenericLaunchFn fn = lookup_generic(num_blocks, has_delta, has_onorm);
       if (fn == nullptr) return ATTN_RES_EINVAL;
       e = fn(p, T, H, pdl, static_cast<cudaStream_t>(stream));
+    } else if (plan.kernel == ATTN_RES_KERNEL_ROW || plan.kernel == ATTN_RES_KERNEL_ROW_SMEM) {
+      RowLaunchFn fn = (plan.kernel == ATTN_RES_KERNEL_ROW ? lookup_row : lookup_row_smem)(
+          num_blocks, row_vpt_index(plan.vpt), has_delta, has_onorm);
+      if (fn == nullptr) return ATTN_RES_EINVAL;
+      e = fn(p, T, pdl, static_cast<cudaStream_t>(stream));
     } else if (plan.kernel == ATTN_RES_KERNEL_SPLIT) {
       const int idx = H == kH ? split_index(plan.split) : kAnyWidthSplitIndex;
       LaunchFn fn = lookup(num_blocks, idx, has_delta, has_onorm);
@@ -681,7 +817,7 @@ const char* attn_res_status_string(attn_res_status_t s) {
 int attn_res_hidden_size(void) { return ATTN_RES_HIDDEN; }
 int attn_res_max_blocks(void) { return ATTN_RES_MAX_BLOCKS; }
 
-attn_res_status_t attn_res_launch_shape(int64_t T, int num_blocks,
+attn_res_status_t attn_res_launch_shape(int64_t T, int num_blocks, int has_delta,
                                         int has_out_norm, uint32_t flags,
                                         int* kernel, int* split, int* stages,
                                         int* threads_per_cta, int64_t* ctas,
@@ -692,14 +828,34 @@ attn_res_status_t attn_res_launch_shape(int64_t T, int num_blocks,
   attn_res_status_t st = make_plan(T, num_blocks, has_out_norm != 0, flags, false, &pl);
   if (st != ATTN_RES_OK) return st;
   const bool comm = num_blocks > 0 || has_out_norm;
-  const bool generic = pl.kernel == ATTN_RES_KERNEL_GENERIC;
+  int th = 0, depth = 0, cl = 1;
+  int64_t grid = 0;
+  switch (pl.kernel) {
+    case ATTN_RES_KERNEL_GENERIC:
+      th = attn_res_dev::kGenericThreads, grid = T;
+      break;
+    case ATTN_RES_KERNEL_ROW:
+    case ATTN_RES_KERNEL_ROW_SMEM:
+      th = attn_res_dev::kNV / pl.vpt, grid = T;
+      break;
+    case ATTN_RES_KERNEL_SPLIT:
+      th = threads_for(pl.split, pl.vpt), grid = T * pl.split, cl = comm ? pl.split : 1;
+      break;
+    case ATTN_RES_KERNEL_STAGED:
+      depth = staged_stages(kStreamShapes[pl.shape], num_blocks, has_delta != 0);
+      if (depth < 2) return ATTN_RES_EINVAL;
+      th = threads_for(pl.split, pl.vpt), cl = comm ? pl.split : 1;
+      break;
+    default:  // the stream kernel
+      th = threads_for(pl.split, pl.vpt), depth = pl.stages, cl = comm ? pl.split : 1;
+      break;
+  }
   if (kernel) *kernel = pl.kernel;
   if (split) *split = pl.split;
-  if (stages) *stages = pl.stages;
-  if (threads_per_cta)
-    *threads_per_cta = generic ? attn_res_dev::kGenericThreads : threads_for(pl.split, pl.vpt);
-  if (ctas) *ctas = pl.kernel == ATTN_RES_KERNEL_STREAM ? 0 : T * pl.split;
-  if (cluster) *cluster = (comm && !generic) ? pl.split : 1;
+  if (stages) *stages = depth;
+  if (threads_per_cta) *threads_per_cta = th;
+  if (ctas) *ctas = grid;
+  if (cluster) *cluster = cl;
   return ATTN_RES_OK;
 }
 

@@ -1,6 +1,8 @@
 // attn_res_inst.cu -- every specialisation for one num_blocks value.
 // Compiled once per S in 0..8 with -DATTN_RES_S=<S>, so the 9 translation
 // units build in parallel.
+#include <utility>
+
 #include "attn_res_launch.cuh"
 
 #ifndef ATTN_RES_S
@@ -34,6 +36,20 @@ LaunchFn ATTN_RES_CAT(launcher_s, ATTN_RES_S)(int split_idx, bool d, bool o) {
 }
 
 namespace {
+// A staged shape exists for this S and delta only if two stages fit.
+template <int SH, bool D>
+StreamLaunchFn pick_staged(bool o) {
+  constexpr int S = ATTN_RES_S;
+  constexpr StreamShape sh = kStreamShapes[SH];
+  constexpr int ST = staged_stages(sh, S, D);
+  if constexpr (ST < 2) {
+    return nullptr;
+  } else {
+    return o ? &launch_stream<S, D, true, sh.k, sh.vpt, ST, sh.grouped, true>
+             : &launch_stream<S, D, false, sh.k, sh.vpt, ST, sh.grouped, true>;
+  }
+}
+
 template <int SH>
 StreamLaunchFn pick_stream(bool d, bool o) {
   constexpr int S = ATTN_RES_S;
@@ -41,26 +57,66 @@ StreamLaunchFn pick_stream(bool d, bool o) {
   constexpr int V = kStreamShapes[SH].vpt;
   constexpr int ST = kStreamShapes[SH].stages;
   constexpr bool G = kStreamShapes[SH].grouped;
-  if (d) return o ? &launch_stream<S, true, true, K, V, ST, G> : &launch_stream<S, true, false, K, V, ST, G>;
-  return o ? &launch_stream<S, false, true, K, V, ST, G> : &launch_stream<S, false, false, K, V, ST, G>;
+  if constexpr (kStreamShapes[SH].staged) {
+    return d ? pick_staged<SH, true>(o) : pick_staged<SH, false>(o);
+  } else {
+    if (d) return o ? &launch_stream<S, true, true, K, V, ST, G> : &launch_stream<S, true, false, K, V, ST, G>;
+    return o ? &launch_stream<S, false, true, K, V, ST, G> : &launch_stream<S, false, false, K, V, ST, G>;
+  }
+}
+
+template <int... I>
+StreamLaunchFn pick_stream_at(int shape_idx, bool d, bool o, std::integer_sequence<int, I...>) {
+  StreamLaunchFn fn = nullptr;
+  ((shape_idx == I ? (fn = pick_stream<I>(d, o), 0) : 0), ...);
+  return fn;
 }
 }  // namespace
 
 StreamLaunchFn ATTN_RES_CAT(stream_launcher_s, ATTN_RES_S)(int shape_idx, bool d, bool o) {
-  static_assert(kNumStreamShapes == 11, "update the switch below");
-  switch (shape_idx) {
-    case 0: return pick_stream<0>(d, o);
-    case 1: return pick_stream<1>(d, o);
-    case 2: return pick_stream<2>(d, o);
-    case 3: return pick_stream<3>(d, o);
-    case 4: return pick_stream<4>(d, o);
-    case 5: return pick_stream<5>(d, o);
-    case 6: return pick_stream<6>(d, o);
-    case 7: return pick_stream<7>(d, o);
-    case 8: return pick_stream<8>(d, o);
-    case 9: return pick_stream<9>(d, o);
-    case 10: return pick_stream<10>(d, o);
-    default: return nullptr;
+  return pick_stream_at(shape_idx, d, o, std::make_integer_sequence<int, kNumStreamShapes>{});
+}
+
+namespace {
+template <int V>
+RowLaunchFn pick_row(bool d, bool o) {
+  constexpr int S = ATTN_RES_S;
+  if (d) return o ? &launch_row<S, true, true, V> : &launch_row<S, true, false, V>;
+  return o ? &launch_row<S, false, true, V> : &launch_row<S, false, false, V>;
+}
+}  // namespace
+
+RowLaunchFn ATTN_RES_CAT(row_launcher_s, ATTN_RES_S)(int vpt_idx, bool d, bool o) {
+  static_assert(kNumRowVpts == 2, "update the switch below");
+  if constexpr (ATTN_RES_S > kRowMaxBlocks) {
+    return nullptr;
+  } else {
+    switch (vpt_idx) {
+      case 0: return pick_row<kRowVpts[0]>(d, o);
+      case 1: return pick_row<kRowVpts[1]>(d, o);
+      default: return nullptr;
+    }
+  }
+}
+
+namespace {
+template <int V>
+RowLaunchFn pick_row_smem(bool d, bool o) {
+  constexpr int S = ATTN_RES_S;
+  if (d) return o ? &launch_row_smem<S, true, true, V> : &launch_row_smem<S, true, false, V>;
+  return o ? &launch_row_smem<S, false, true, V> : &launch_row_smem<S, false, false, V>;
+}
+}  // namespace
+
+RowLaunchFn ATTN_RES_CAT(row_smem_launcher_s, ATTN_RES_S)(int vpt_idx, bool d, bool o) {
+  if constexpr (ATTN_RES_S < kRowSmemMinBlocks || ATTN_RES_S > kRowSmemMaxBlocks) {
+    return nullptr;
+  } else {
+    switch (vpt_idx) {
+      case 0: return pick_row_smem<kRowVpts[0]>(d, o);
+      case 1: return pick_row_smem<kRowVpts[1]>(d, o);
+      default: return nullptr;
+    }
   }
 }
 

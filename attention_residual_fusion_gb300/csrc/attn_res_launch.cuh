@@ -6,6 +6,7 @@
 #include <cstdint>
 
 #include "attn_res_kernel.cuh"
+#include "attn_res_row.cuh"
 #include "attn_res_stream.cuh"
 #include "attn_res_generic.cuh"
 #include "attn_res_tp.cuh"
@@ -73,29 +74,45 @@ cudaError_t launch_split(const Params& p, int64_t T, bool pdl,
 }
 
 // Shapes the persistent stream kernel is built for: CTAs per token row (K),
-// 16-byte vectors per thread and per row (VPT), ring depth (STAGES).
+// 16-byte vectors per thread and per row (VPT), ring depth (STAGES).  Staged
+// shapes (prefix and delta in the ring too) give CTAs per SM in place of the
+// depth; their depth follows from the rows of a stage (staged_depth).
 struct StreamShape {
   int k, vpt, stages;
   bool grouped;  // built for B > 1 token rows per bank row
+  bool staged;   // prefix and delta staged in the ring; `stages` = CTAs per SM
 };
 // The next-to-last entry is the one shape built for shared bank rows (B > 1);
 // the last (k = 0) serves any width H that is a multiple of 1024: H / 1024
 // CTAs per token row, each with the per-CTA layout of (7,2,2), shared bank
 // rows allowed.
-constexpr StreamShape kStreamShapes[] = {{7, 1, 2, false}, {7, 2, 2, false}, {7, 2, 3, false},
-                                         {7, 4, 2, false}, {4, 2, 2, false}, {4, 2, 3, false},
-                                         {2, 4, 2, false}, {14, 2, 2, false}, {2, 8, 2, false},
-                                         {7, 2, 2, true},  {0, 2, 2, true}};
+constexpr StreamShape kStreamShapes[] = {
+    {7, 1, 2, false, false}, {7, 2, 2, false, false}, {7, 2, 3, false, false},
+    {7, 4, 2, false, false}, {4, 2, 2, false, false}, {4, 2, 3, false, false},
+    {2, 4, 2, false, false}, {14, 2, 2, false, false}, {2, 8, 2, false, false},
+    {4, 4, 5, false, true},  {7, 4, 7, false, true},  {4, 4, 4, false, true},
+    {7, 2, 2, true, false},  {0, 2, 2, true, false}};
 constexpr int kNumStreamShapes = sizeof(kStreamShapes) / sizeof(kStreamShapes[0]);
 constexpr int kGroupedStreamShape = kNumStreamShapes - 2;
 constexpr int kAnyWidthStreamShape = kNumStreamShapes - 1;
 
-inline int stream_shape_index(int k, int vpt, int stages, bool grouped) {
+inline int stream_shape_index(int k, int vpt, int stages, bool grouped, bool staged) {
   for (int i = 0; i < kNumStreamShapes; ++i)
     if (kStreamShapes[i].k == k && kStreamShapes[i].vpt == vpt &&
-        kStreamShapes[i].stages == stages && kStreamShapes[i].grouped == grouped)
+        kStreamShapes[i].stages == stages && kStreamShapes[i].grouped == grouped &&
+        kStreamShapes[i].staged == staged)
       return i;
   return -1;
+}
+
+// Ring depth of staged shape `sh` for num_blocks bank rows (with or without
+// delta); < 2 means the shape does not exist for them.
+constexpr int staged_stages(const StreamShape& sh, int num_blocks, bool has_delta) {
+  const int vpc = attn_res_dev::kNV / sh.k;
+  const int nw = (vpc / sh.vpt + 31) / 32;
+  return attn_res_dev::staged_depth(num_blocks + (has_delta ? 2 : 1), (uint32_t)vpc * 16u,
+                                    sh.stages,
+                                    attn_res_dev::stream_static_bytes(num_blocks, sh.k, nw));
 }
 
 // Enqueue the persistent kernel: as many clusters as fit on the device at
@@ -103,11 +120,12 @@ inline int stream_shape_index(int k, int vpt, int stages, bool grouped) {
 using StreamLaunchFn = cudaError_t (*)(const Params&, int64_t T, bool pdl,
                                        cudaStream_t stream, int device, int kc);
 
-template <int S, bool D, bool O, int K, int VPT, int STAGES, bool G>
+template <int S, bool D, bool O, int K, int VPT, int STAGES, bool G, bool STAGED = false>
 cudaError_t launch_stream(const Params& p, int64_t T, bool pdl, cudaStream_t stream,
                           int device, int kc) {
-  using C = attn_res_dev::StreamCfg<S, D, O, K, VPT, STAGES>;
-  void (*kern)(Params, int64_t) = attn_res_dev::attn_res_stream_kernel<S, D, O, K, VPT, STAGES, G>;
+  using C = attn_res_dev::StreamCfg<S, D, O, K, VPT, STAGES, STAGED>;
+  void (*kern)(Params, int64_t) =
+      attn_res_dev::attn_res_stream_kernel<S, D, O, K, VPT, STAGES, G, STAGED>;
   // any width not a multiple of 1024: the entry point with a short last slice
   int ragged = 0;
   if constexpr (K == 0) {
@@ -180,6 +198,71 @@ cudaError_t launch_stream(const Params& p, int64_t T, bool pdl, cudaStream_t str
   cfg.attrs = attrs;
   cfg.numAttrs = n;
   return cudaLaunchKernelEx(&cfg, kern, p, T);
+}
+
+// The row kernel: one CTA per token row (the whole row), VPT vectors per
+// thread, built for up to kRowMaxBlocks bank rows (its rows live in
+// registers; more rows leave one CTA per SM or spill).  Supported VPT
+// values, in table order.
+constexpr int kRowMaxBlocks = 2;
+constexpr int kRowVpts[] = {4, 7};
+constexpr int kNumRowVpts = sizeof(kRowVpts) / sizeof(kRowVpts[0]);
+
+inline int row_vpt_index(int vpt) {
+  for (int i = 0; i < kNumRowVpts; ++i)
+    if (kRowVpts[i] == vpt) return i;
+  return -1;
+}
+
+using RowLaunchFn = cudaError_t (*)(const Params&, int64_t T, bool pdl, cudaStream_t stream);
+
+template <int S, bool D, bool O, int VPT>
+cudaError_t launch_row(const Params& p, int64_t T, bool pdl, cudaStream_t stream) {
+  using C = attn_res_dev::RowCfg<S, D, O, VPT>;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(T), 1, 1);
+  cfg.blockDim = dim3(C::THREADS, 1, 1);
+  cfg.stream = stream;
+  cfg.attrs = &attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, attn_res_dev::attn_res_row_kernel<S, D, O, VPT>, p);
+}
+
+// The row kernel with its rows in shared memory: built for kRowSmemMinBlocks
+// .. kRowSmemMaxBlocks bank rows (two CTAs of up to 7 rows fit an SM).
+constexpr int kRowSmemMinBlocks = 1;
+constexpr int kRowSmemMaxBlocks = 5;
+
+template <int S, bool D, bool O, int VPT>
+cudaError_t launch_row_smem(const Params& p, int64_t T, bool pdl, cudaStream_t stream) {
+  using C = attn_res_dev::RowCfg<S, D, O, VPT>;
+  void (*kern)(Params) = attn_res_dev::attn_res_row_smem_kernel<S, D, O, VPT>;
+  int device = 0;
+  cudaError_t e = cudaGetDevice(&device);
+  if (e != cudaSuccess) return e;
+  if (device < 0 || device >= 64) return cudaErrorInvalidValue;
+  // the dynamic shared memory above 48 KB is opt-in, per function and device
+  static std::atomic<uint64_t> enabled{0};
+  const uint64_t bit = 1ull << device;
+  if (!(enabled.load(std::memory_order_acquire) & bit)) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    enabled.fetch_or(bit, std::memory_order_acq_rel);
+  }
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(T), 1, 1);
+  cfg.blockDim = dim3(C::THREADS, 1, 1);
+  cfg.dynamicSmemBytes = C::SMEM_BYTES;
+  cfg.stream = stream;
+  cfg.attrs = &attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
 // The general kernel: one CTA per token row, any H that is a multiple of 8.
@@ -313,6 +396,25 @@ StreamLaunchFn stream_launcher_s5(int shape_idx, bool d, bool o);
 StreamLaunchFn stream_launcher_s6(int shape_idx, bool d, bool o);
 StreamLaunchFn stream_launcher_s7(int shape_idx, bool d, bool o);
 StreamLaunchFn stream_launcher_s8(int shape_idx, bool d, bool o);
+
+RowLaunchFn row_smem_launcher_s0(int vpt_idx, bool d, bool o);
+RowLaunchFn row_smem_launcher_s1(int vpt_idx, bool d, bool o);
+RowLaunchFn row_smem_launcher_s2(int vpt_idx, bool d, bool o);
+RowLaunchFn row_smem_launcher_s3(int vpt_idx, bool d, bool o);
+RowLaunchFn row_smem_launcher_s4(int vpt_idx, bool d, bool o);
+RowLaunchFn row_smem_launcher_s5(int vpt_idx, bool d, bool o);
+RowLaunchFn row_smem_launcher_s6(int vpt_idx, bool d, bool o);
+RowLaunchFn row_smem_launcher_s7(int vpt_idx, bool d, bool o);
+RowLaunchFn row_smem_launcher_s8(int vpt_idx, bool d, bool o);
+RowLaunchFn row_launcher_s0(int vpt_idx, bool d, bool o);
+RowLaunchFn row_launcher_s1(int vpt_idx, bool d, bool o);
+RowLaunchFn row_launcher_s2(int vpt_idx, bool d, bool o);
+RowLaunchFn row_launcher_s3(int vpt_idx, bool d, bool o);
+RowLaunchFn row_launcher_s4(int vpt_idx, bool d, bool o);
+RowLaunchFn row_launcher_s5(int vpt_idx, bool d, bool o);
+RowLaunchFn row_launcher_s6(int vpt_idx, bool d, bool o);
+RowLaunchFn row_launcher_s7(int vpt_idx, bool d, bool o);
+RowLaunchFn row_launcher_s8(int vpt_idx, bool d, bool o);
 
 GenericLaunchFn generic_launcher_s0(bool d, bool o);
 GenericLaunchFn generic_launcher_s1(bool d, bool o);

@@ -45,7 +45,33 @@ namespace attn_res_dev {
 constexpr int kRtCols = 1024;
 constexpr int kRtMaxK = 16;
 
-template <int S, bool HAS_DELTA, bool HAS_ONORM, int K, int VPT, int STAGES>
+// Ring depth of the staged form (STAGED below): as many stages of `rows` row
+// slices of `slice_bytes` each as fit when `ctas_per_sm` CTAs share an SM's
+// 228 KB of shared memory, each also holding `static_bytes` of static shared
+// memory (mailboxes, barriers) and the 1 KB the system reserves, and within
+// the 227 KB one CTA may have; at most kStagedMaxStages.  Below 2 the form
+// does not exist for that row count.
+constexpr int kStagedMaxStages = 8;
+__host__ __device__ constexpr int staged_depth(int rows, uint32_t slice_bytes, int ctas_per_sm,
+                                               uint32_t static_bytes) {
+  const uint32_t per_cta = 233472u / (uint32_t)ctas_per_sm - 1024u - static_bytes;
+  const uint32_t cap = 232448u - static_bytes;
+  const int n = (int)((per_cta < cap ? per_cta : cap) / ((uint32_t)rows * slice_bytes));
+  return n < kStagedMaxStages ? n : kStagedMaxStages;
+}
+// Static shared memory of a stream CTA: the mailboxes of K CTAs x NW warps
+// for S bank rows, and a full and an empty barrier per stage (at most
+// kStagedMaxStages).
+__host__ __device__ constexpr uint32_t stream_static_bytes(int S, int K, int NW) {
+  return (uint32_t)(2 * K * NW * 2 * (S + 1) * 4 + 2 * K * NW * 4 + 32) + 16u * kStagedMaxStages;
+}
+
+// STAGED: the ring holds the token's prefix and delta slices as well as its
+// bank rows (one stage = S bank rows, prefix, delta), all brought in by bulk
+// copies, so no row data waits in registers and the depth is limited by
+// shared memory alone.  Without it the ring holds bank rows only and each
+// thread loads its prefix and delta vectors into registers one token ahead.
+template <int S, bool HAS_DELTA, bool HAS_ONORM, int K, int VPT, int STAGES, bool STAGED = false>
 struct StreamCfg {
   static constexpr int VPC = K ? kNV / K : kRtCols / kVec;  // vectors per CTA per row
   static constexpr int THREADS = (VPC / VPT + 31) / 32 * 32;
@@ -53,7 +79,11 @@ struct StreamCfg {
   using Tok = TokenCfg<S, HAS_DELTA, HAS_ONORM, K ? K : kRtMaxK, NW>;
   static constexpr bool COMM = Tok::COMM;
   static constexpr uint32_t SLICE_BYTES = VPC * 16;  // one row's slice, multiple of 16
-  static constexpr uint32_t STAGE_BYTES = S * SLICE_BYTES;
+  // row slices per stage: bank rows, then (staged) prefix and delta
+  static constexpr int RING_ROWS = S + (STAGED ? (HAS_DELTA ? 2 : 1) : 0);
+  static constexpr int PREFIX_ROW = S;       // staged: ring row of the prefix slice
+  static constexpr int DELTA_ROW = S + 1;    // staged with delta: ring row of the delta slice
+  static constexpr uint32_t STAGE_BYTES = RING_ROWS * SLICE_BYTES;
   static constexpr uint32_t SMEM_BYTES = STAGES * STAGE_BYTES;
   // CTAs per SM that shared memory allows (ring, mailboxes, barriers and the
   // 1 KB the system reserves per CTA, out of 228 KB), but never so many that
@@ -63,13 +93,18 @@ struct StreamCfg {
   static constexpr uint32_t SMEM_PER_CTA =
       SMEM_BYTES + sizeof(typename Tok::Box) + 16 * STAGES + 1024;
   static constexpr int BY_SMEM = (int)(233472u / SMEM_PER_CTA);
-  static constexpr int REG_FLOOR = (64 + 48 * VPT) < 255 ? (64 + 48 * VPT) : 255;
+  static constexpr int REG_FLOOR = (64 + (STAGED ? 40 : 48) * VPT) < 255
+                                       ? (64 + (STAGED ? 40 : 48) * VPT) : 255;
   static constexpr int BY_REGS = 65536 / (THREADS * REG_FLOOR);
   static constexpr int MIN_BLOCKS_RAW = BY_SMEM < BY_REGS ? BY_SMEM : BY_REGS;
   static constexpr int MIN_BLOCKS = MIN_BLOCKS_RAW < 1 ? 1 : MIN_BLOCKS_RAW;
   static_assert(K == 0 || kNV % K == 0, "split must divide the 896 row vectors");
   static_assert(VPC % VPT == 0, "vectors per thread must divide the slice");
-  static_assert(STAGES >= 2 && STAGES <= 4, "ring depth");
+  static_assert(STAGES >= 2 && STAGES <= (STAGED ? kStagedMaxStages : 4), "ring depth");
+  static_assert(sizeof(typename Tok::Box) + 16 * STAGES <= stream_static_bytes(S, K ? K : kRtMaxK, NW),
+                "static shared memory above the staged-depth estimate");
+  static_assert(!STAGED || K != 0, "the staged form is built for the 7168 split only");
+  static_assert(RING_ROWS <= 32, "one issuing lane per ring row");
 };
 
 // GROUPED: B token rows per bank row with B > 1 possible (else B == 1 and the
@@ -78,17 +113,18 @@ struct StreamCfg {
 // loads and stores past H are predicated off, its bank-row copies shortened,
 // and the tail of its stage slots zeroed.  Without RAGGED every vector of a
 // slice is in the row, as the tuned shapes need.
-template <int S, bool HAS_DELTA, bool HAS_ONORM, int K, int VPT, int STAGES, bool GROUPED, bool RAGGED>
+template <int S, bool HAS_DELTA, bool HAS_ONORM, int K, int VPT, int STAGES, bool GROUPED,
+          bool RAGGED, bool STAGED>
 __device__ __forceinline__ void stream_body(const Params& p, const int64_t T) {
   static_assert(K == 0 || !RAGGED, "only the any-width form has a short last slice");
-  using C = StreamCfg<S, HAS_DELTA, HAS_ONORM, K, VPT, STAGES>;
+  using C = StreamCfg<S, HAS_DELTA, HAS_ONORM, K, VPT, STAGES, STAGED>;
   using Tok = typename C::Tok;
   constexpr int VPC = C::VPC;
   constexpr int THREADS = C::THREADS;
   constexpr int NW = C::NW;
   constexpr bool COMM = C::COMM;
 
-  extern __shared__ __align__(128) uint4 ring[];  // [STAGES][S][VPC]
+  extern __shared__ __align__(128) uint4 ring[];  // [STAGES][RING_ROWS][VPC]
   __shared__ __align__(8) unsigned long long full_bar[STAGES];
   __shared__ __align__(8) unsigned long long empty_bar[STAGES];
   __shared__ typename Tok::Box mb;
@@ -134,7 +170,7 @@ __device__ __forceinline__ void stream_body(const Params& p, const int64_t T) {
   // sums and the mix see zero columns there
   if (RAGGED && slice_bytes < C::SLICE_BYTES) {
     const int tail = (int)(C::SLICE_BYTES - slice_bytes) / 16;
-    for (int e = tid; e < STAGES * S * tail; e += THREADS)
+    for (int e = tid; e < STAGES * C::RING_ROWS * tail; e += THREADS)
       ring[(e / tail) * VPC + (int)(slice_bytes / 16) + e % tail] = make_uint4(0, 0, 0, 0);
   }
   if (COMM) {
@@ -144,17 +180,29 @@ __device__ __forceinline__ void stream_body(const Params& p, const int64_t T) {
   }
 
   // producer side (every lane of warp 0): the bank rows of one token into one
-  // stage -- lane 0 arms the stage's barrier with the byte count, then lane i
-  // < S issues the copy of bank row i, so the S copies go out as one warp
-  // instruction
+  // stage -- lane 0 arms the stage's barrier with the byte count of the whole
+  // stage, then lane i < S issues the copy of bank row i, so the S copies go
+  // out as one warp instruction; staged, lanes S and S + 1 copy the prefix
+  // and delta slices (issue_current), after the grid-dependency wait
   auto issue_bank = [&](int64_t t, int s) {
     const uint32_t bar = smem_addr(&full_bar[s]);
-    if (lane == 0) mbar_arrive_expect_tx(bar, RAGGED ? S * slice_bytes : C::STAGE_BYTES);
+    if (lane == 0) mbar_arrive_expect_tx(bar, RAGGED ? C::RING_ROWS * slice_bytes : C::STAGE_BYTES);
     __syncwarp();
     if (lane < S)
-      bulk_load(ring_addr + (uint32_t)(s * S + lane) * C::SLICE_BYTES,
+      bulk_load(ring_addr + (uint32_t)(s * C::RING_ROWS + lane) * C::SLICE_BYTES,
                 bank_of<GROUPED>(p, t) + slice0 + (int64_t)lane * p.blocks_slot,
                 RAGGED ? slice_bytes : C::SLICE_BYTES, bar);
+  };
+  auto issue_current = [&](int64_t t, int s) {
+    if constexpr (STAGED) {
+      const uint32_t bar = smem_addr(&full_bar[s]);
+      const uint16_t* src = nullptr;
+      if (lane == C::PREFIX_ROW) src = p.prefix + t * p.prefix_row + slice0;
+      if (HAS_DELTA && lane == C::DELTA_ROW) src = p.delta + t * p.delta_row + slice0;
+      if (src != nullptr)
+        bulk_load(ring_addr + (uint32_t)(s * C::RING_ROWS + lane) * C::SLICE_BYTES, src,
+                  RAGGED ? slice_bytes : C::SLICE_BYTES, bar);
+    }
   };
   // every thread: its vectors of the token's prefix and delta rows
   auto load_current = [&](int64_t t, uint4 (&pre)[VPT], uint4 (&del)[VPT]) {
@@ -185,14 +233,21 @@ __device__ __forceinline__ void stream_body(const Params& p, const int64_t T) {
   for (int v = 0; v < VPT; ++v) {
     rw[v] = qw[v] = ow[v] = make_uint4(0, 0, 0, 0);
     if (active[v]) {
-      rw[v] = ld_weight(p.rms_w + col[v]);
-      qw[v] = ld_weight(p.res_w + col[v]);
+      if (S > 0) {  // the query only enters the logits
+        rw[v] = ld_weight(p.rms_w + col[v]);
+        qw[v] = ld_weight(p.res_w + col[v]);
+      }
       if (HAS_ONORM) ow[v] = ld_weight(p.onw + col[v]);
     }
   }
   grid_dep_wait();  // every thread: also orders our stores after the producer's work
   uint4 pre[VPT], del[VPT];  // prefix and delta of the next token to start
-  if (ntok > 0) load_current(cid, pre, del);
+  if constexpr (STAGED) {
+    if (warp == 0)
+      for (int s = 0; s < STAGES && s < ntok; ++s) issue_current(cid + s * ncl, s);
+  } else {
+    if (ntok > 0) load_current(cid, pre, del);
+  }
 
   f32x2 q[VPT][4];
   make_query<VPT>(rw, qw, q);
@@ -202,20 +257,31 @@ __device__ __forceinline__ void stream_body(const Params& p, const int64_t T) {
   // (phases in attn_res_token.cuh).  A peer runs at most one token ahead,
   // which the double-buffered mailboxes allow.
   bool failed = false;
-  auto stage_of = [&](int64_t j) { return ring + (int)(j % STAGES) * S * VPC + tid; };
+  auto stage_of = [&](int64_t j) { return ring + (int)(j % STAGES) * C::RING_ROWS * VPC + tid; };
   // A(j): current row; then, its prefix/delta registers free, the next
   // token's prefix/delta loads go out; then the partial sums.
   auto phase_a = [&](int64_t j, uint4 (&cc)[VPT]) {
     const int s = (int)(j % STAGES);
     const int b = (int)(j & 1);
     if (COMM && tid == 0) mailbox_expect<Tok>(mb, b, HAS_ONORM, sp);
-    current_row<HAS_DELTA, VPT>(pre, del, cc);
-    if (j + 1 < ntok) load_current(cid + (j + 1) * ncl, pre, del);
+    if constexpr (!STAGED) {
+      current_row<HAS_DELTA, VPT>(pre, del, cc);
+      if (j + 1 < ntok) load_current(cid + (j + 1) * ncl, pre, del);
+    }
     const bool was_failed = failed;
     wait_or_flag(smem_addr(&full_bar[s]), (uint32_t)((j / STAGES) & 1), failed, p.err,
                  kErrStageTimeout);
     if (tid == 0 && !was_failed && !failed) pending &= ~(1u << s);
     const uint4* stage = stage_of(j);
+    if constexpr (STAGED) {
+#pragma unroll
+      for (int v = 0; v < VPT; ++v) {
+        const bool on = RAGGED || active[v];
+        pre[v] = on ? stage[C::PREFIX_ROW * VPC + v * THREADS] : make_uint4(0, 0, 0, 0);
+        del[v] = (on && HAS_DELTA) ? stage[C::DELTA_ROW * VPC + v * THREADS] : make_uint4(0, 0, 0, 0);
+      }
+      current_row<HAS_DELTA, VPT>(pre, del, cc);
+    }
     token_sums<S, HAS_DELTA, HAS_ONORM, (K ? K : kRtMaxK), NW, VPT>(
         [&](int i, int v) { return (RAGGED || active[v]) ? stage[i * VPC + v * THREADS] : make_uint4(0, 0, 0, 0); },
         cc, q, mb, b, rank, warp, lane, sp);
@@ -256,6 +322,7 @@ __device__ __forceinline__ void stream_body(const Params& p, const int64_t T) {
       if (go) {
         fence_proxy_async_smem();
         issue_bank(cid + (j + STAGES) * ncl, s);
+        issue_current(cid + (j + STAGES) * ncl, s);
         pending |= 1u << s;
         pending_parity = (pending_parity & ~(1u << s)) | ((sparity ^ 1u) << s);
       }
@@ -298,11 +365,12 @@ __device__ __forceinline__ void stream_body(const Params& p, const int64_t T) {
   }
 }
 
-template <int S, bool HAS_DELTA, bool HAS_ONORM, int K, int VPT, int STAGES, bool GROUPED>
-__global__ void __launch_bounds__(StreamCfg<S, HAS_DELTA, HAS_ONORM, K, VPT, STAGES>::THREADS,
-                                  StreamCfg<S, HAS_DELTA, HAS_ONORM, K, VPT, STAGES>::MIN_BLOCKS)
+template <int S, bool HAS_DELTA, bool HAS_ONORM, int K, int VPT, int STAGES, bool GROUPED,
+          bool STAGED>
+__global__ void __launch_bounds__(StreamCfg<S, HAS_DELTA, HAS_ONORM, K, VPT, STAGES, STAGED>::THREADS,
+                                  StreamCfg<S, HAS_DELTA, HAS_ONORM, K, VPT, STAGES, STAGED>::MIN_BLOCKS)
     attn_res_stream_kernel(const Params p, const int64_t T) {
-  stream_body<S, HAS_DELTA, HAS_ONORM, K, VPT, STAGES, GROUPED, false>(p, T);
+  stream_body<S, HAS_DELTA, HAS_ONORM, K, VPT, STAGES, GROUPED, false, STAGED>(p, T);
 }
 
 // Any width H that is not a multiple of kRtCols (the last CTA's slice short).
@@ -310,7 +378,7 @@ template <int S, bool HAS_DELTA, bool HAS_ONORM, int VPT, int STAGES, bool GROUP
 __global__ void __launch_bounds__(StreamCfg<S, HAS_DELTA, HAS_ONORM, 0, VPT, STAGES>::THREADS,
                                   StreamCfg<S, HAS_DELTA, HAS_ONORM, 0, VPT, STAGES>::MIN_BLOCKS)
     attn_res_stream_ragged_kernel(const Params p, const int64_t T) {
-  stream_body<S, HAS_DELTA, HAS_ONORM, 0, VPT, STAGES, GROUPED, true>(p, T);
+  stream_body<S, HAS_DELTA, HAS_ONORM, 0, VPT, STAGES, GROUPED, true, false>(p, T);
 }
 
 }  // namespace attn_res_dev

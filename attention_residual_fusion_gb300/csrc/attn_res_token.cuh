@@ -34,14 +34,14 @@ struct Mailbox {
   unsigned long long bar_sq[2];
 };
 
-template <int S, bool HAS_DELTA, bool HAS_ONORM, int K, int NW>
-struct TokenCfg {
+// The 2N per-source sums of a token (sum(x_i^2), then <x_i, q>) as a warp
+// reduces them: one power-of-two butterfly of P values, plus a second one of
+// P2 values when NR is just above a power of two (NR = 18 for S = 8 reduces
+// as 16 + 2 instead of a padded 32).
+template <int S>
+struct SumsCfg {
   static constexpr int N = S + 1;              // sources
   static constexpr int NR = 2 * N;             // partial sums per token
-  static constexpr int ROWS = N + (HAS_DELTA ? 1 : 0);
-  // The partial sums reduce as one power-of-two butterfly of P values, plus
-  // a second one of P2 values when NR is just above a power of two (NR = 18
-  // for S = 8 reduces as 16 + 2 instead of a padded 32).
   static constexpr int P_FULL = pow2_at_least(NR);
   static constexpr int P = (NR > 16) ? 16 : P_FULL;
   static constexpr int NR2 = NR - P > 0 ? NR - P : 0;  // values in the second butterfly
@@ -49,6 +49,20 @@ struct TokenCfg {
   static constexpr int SHIFT = 5 - log2_exact(P);
   static constexpr int SHIFT2 = 5 - log2_exact(P2);
   static_assert(NR2 <= 16, "second butterfly too large");
+  static_assert(NR <= 32, "one lane per sum");
+};
+
+template <int S, bool HAS_DELTA, bool HAS_ONORM, int K, int NW>
+struct TokenCfg : SumsCfg<S> {
+  using Sums = SumsCfg<S>;
+  using Sums::N;
+  using Sums::NR;
+  using Sums::P;
+  using Sums::NR2;
+  using Sums::P2;
+  using Sums::SHIFT;
+  using Sums::SHIFT2;
+  static constexpr int ROWS = N + (HAS_DELTA ? 1 : 0);
   static constexpr uint32_t SUMS_BYTES = K * NW * NR * 4;  // expected per token
   static constexpr uint32_t SQ_BYTES = K * NW * 4;
   static constexpr bool COMM = (S > 0) || HAS_ONORM;
@@ -111,63 +125,160 @@ __device__ __forceinline__ void current_row(const uint4 (&pre)[VPT], const uint4
   for (int v = 0; v < VPT; ++v) c[v] = HAS_DELTA ? add_bf16x8(pre[v], del[v]) : pre[v];
 }
 
+// ---- per-token building blocks (any transport of the sums) ----------------------
 // row(i, v): vector v of bank row i < S; c: the current-layer row (the last
 // source).
+
+// The thread's partial sums over its VPT vectors of every source, reduced
+// over the warp.  On return lane l holds in `lo` the warp total of sum
+// l >> SHIFT (meaningful where lo_holder(l)) and in `hi` the total of sum
+// P + (l >> SHIFT2) (where hi_holder(l)).
+template <int S, int VPT, class Row>
+__device__ __forceinline__ void warp_sums(Row row, const uint4 (&c)[VPT], const f32x2 (&q)[VPT][4],
+                                          int lane, float& lo, float& hi) {
+  using C = SumsCfg<S>;
+  constexpr int N = C::N;
+  constexpr int P = C::P;
+  constexpr int P2 = C::P2;
+  float part[P + P2];
+#pragma unroll
+  for (int r = 0; r < P + P2; ++r) part[r] = 0.f;
+#pragma unroll
+  for (int i = 0; i < N; ++i) {
+    f32x2 ss = 0ull, dt = 0ull;  // +0.0f pairs
+#pragma unroll
+    for (int v = 0; v < VPT; ++v) {
+      const uint4 xi = (i < S) ? row(i < S ? i : 0, v) : c[v];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const f32x2 x2 = bf2_widen(vword(xi, k));
+        ss = f2_fma(x2, x2, ss);
+        dt = f2_fma(x2, q[v][k], dt);
+      }
+    }
+    part[i] = f2_lo(ss) + f2_hi(ss);
+    part[N + i] = f2_lo(dt) + f2_hi(dt);
+  }
+  float a[P];
+#pragma unroll
+  for (int r = 0; r < P; ++r) a[r] = part[r];
+  lo = reduce_scatter<P>(a, lane);
+  hi = 0.f;
+  if constexpr (C::NR2 > 0) {
+    float b[P2];
+#pragma unroll
+    for (int r = 0; r < P2; ++r) b[r] = part[P + r];
+    hi = reduce_scatter<P2>(b, lane);
+  }
+}
+// Which lanes hold a sum after warp_sums, and its index.
+template <int S>
+__device__ __forceinline__ bool lo_holder(int lane) {
+  using C = SumsCfg<S>;
+  return (lane & ((1 << C::SHIFT) - 1)) == 0 && (lane >> C::SHIFT) < (C::NR < C::P ? C::NR : C::P);
+}
+template <int S>
+__device__ __forceinline__ int lo_index(int lane) { return lane >> SumsCfg<S>::SHIFT; }
+template <int S>
+__device__ __forceinline__ bool hi_holder(int lane) {
+  using C = SumsCfg<S>;
+  return C::NR2 > 0 && (lane & ((1 << C::SHIFT2) - 1)) == 0 && (lane >> C::SHIFT2) < C::NR2;
+}
+template <int S>
+__device__ __forceinline__ int hi_index(int lane) { return SumsCfg<S>::P + (lane >> SumsCfg<S>::SHIFT2); }
+
+// Logits and softmax from the token totals (lane l < NR holds sum l); lane
+// i < N returns w_i.  Reciprocal square root and a fast quotient (z in
+// [1, N]): a few ulp of fp32 on the weights, far below the bf16 output's
+// resolution, and the same instructions in every warp, so the weights are
+// bit-identical wherever they are computed from the same totals.
+template <int S>
+__device__ __forceinline__ float softmax_weight(float tot, int lane, float eps, float inv_h) {
+  constexpr int N = S + 1;
+  const float dtv = __shfl_sync(0xffffffffu, tot, (lane + N) & 31);
+  float logit = __int_as_float(0xff800000u);  // -inf
+  if (lane < N) logit = dtv * rsqrtf(fmaf(tot, inv_h, eps));
+  const float m = warp_max(logit);
+  const float e = (lane < N) ? expf(logit - m) : 0.f;
+  const float z = warp_sum(e);
+  return __fdividef(e, z);
+}
+
+// acc = sum_i w_i x_i over the raw rows; lane i holds w_i in `wl`.
+template <int S, int VPT, class Row>
+__device__ __forceinline__ void mix_rows(Row row, const uint4 (&c)[VPT], float wl,
+                                         f32x2 (&acc)[VPT][4]) {
+  constexpr int N = S + 1;
+#pragma unroll
+  for (int v = 0; v < VPT; ++v)
+#pragma unroll
+    for (int k = 0; k < 4; ++k) acc[v][k] = 0ull;
+#pragma unroll
+  for (int i = 0; i < N; ++i) {
+    const float w = __shfl_sync(0xffffffffu, wl, i);
+    const f32x2 w2 = f2_make(w, w);
+#pragma unroll
+    for (int v = 0; v < VPT; ++v) {
+      const uint4 xi = (i < S) ? row(i < S ? i : 0, v) : c[v];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) acc[v][k] = f2_fma(w2, bf2_widen(vword(xi, k)), acc[v][k]);
+    }
+  }
+}
+
+// The warp's sum of acc^2 over its columns (every lane gets it).
+template <int VPT>
+__device__ __forceinline__ float warp_sq(const f32x2 (&acc)[VPT][4]) {
+  f32x2 sq2 = 0ull;
+#pragma unroll
+  for (int v = 0; v < VPT; ++v)
+#pragma unroll
+    for (int k = 0; k < 4; ++k) sq2 = f2_fma(acc[v][k], acc[v][k], sq2);
+  return warp_sum(f2_lo(sq2) + f2_hi(sq2));
+}
+
+// Output vectors: acc scaled by ro and the norm weights (output norm), or acc
+// itself, rounded to bf16.
+template <bool HAS_ONORM, int VPT>
+__device__ __forceinline__ void pack_out(f32x2 (&acc)[VPT][4], const uint4 (&ow)[VPT], float ro,
+                                         uint4 (&out)[VPT]) {
+  if constexpr (HAS_ONORM) {
+    const f32x2 ro2 = f2_make(ro, ro);
+#pragma unroll
+    for (int v = 0; v < VPT; ++v)
+#pragma unroll
+      for (int k = 0; k < 4; ++k) acc[v][k] = f2_mul(f2_mul(acc[v][k], ro2), bf2_widen(vword(ow[v], k)));
+  }
+#pragma unroll
+  for (int v = 0; v < VPT; ++v)
+    out[v] = make_uint4(pack_bf16x2(f2_lo(acc[v][0]), f2_hi(acc[v][0])),
+                        pack_bf16x2(f2_lo(acc[v][1]), f2_hi(acc[v][1])),
+                        pack_bf16x2(f2_lo(acc[v][2]), f2_hi(acc[v][2])),
+                        pack_bf16x2(f2_lo(acc[v][3]), f2_hi(acc[v][3])));
+}
+
+// ---- the three phases over the cluster's mailboxes -----------------------------
+
 template <int S, bool HAS_DELTA, bool HAS_ONORM, int K, int NW, int VPT, class Row>
 __device__ __forceinline__ void token_sums(Row row, const uint4 (&c)[VPT],
                                            const f32x2 (&q)[VPT][4],
                                            typename TokenCfg<S, HAS_DELTA, HAS_ONORM, K, NW>::Box& mb,
                                            int b, uint32_t rank, int warp, int lane, Split sp) {
-  using C = TokenCfg<S, HAS_DELTA, HAS_ONORM, K, NW>;
-  constexpr int N = C::N;
-  constexpr int NR = C::NR;
-  constexpr int P = C::P;
   if constexpr (S > 0) {
-    // per-source partial sums over this thread's columns
-    constexpr int P2 = C::P2;
-    float part[P + P2];
-#pragma unroll
-    for (int r = 0; r < P + P2; ++r) part[r] = 0.f;
-#pragma unroll
-    for (int i = 0; i < N; ++i) {
-      f32x2 ss = 0ull, dt = 0ull;  // +0.0f pairs
-#pragma unroll
-      for (int v = 0; v < VPT; ++v) {
-        const uint4 xi = (i < S) ? row(i < S ? i : 0, v) : c[v];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const f32x2 x2 = bf2_widen(vword(xi, k));
-          ss = f2_fma(x2, x2, ss);
-          dt = f2_fma(x2, q[v][k], dt);
-        }
-      }
-      part[i] = f2_lo(ss) + f2_hi(ss);
-      part[N + i] = f2_lo(dt) + f2_hi(dt);
-    }
     // warp totals, then into every CTA's mailbox
+    float tv, tv2;
+    warp_sums<S, VPT>(row, c, q, lane, tv, tv2);
     const int src = (int)rank * NW + warp;
     const uint32_t bar = smem_addr(&mb.bar_sums[b]);
-    float lo[P];
-#pragma unroll
-    for (int r = 0; r < P; ++r) lo[r] = part[r];
-    const float tv = reduce_scatter<P>(lo, lane);
-    const int idx = lane >> C::SHIFT;
-    if ((lane & ((1 << C::SHIFT) - 1)) == 0 && idx < (NR < P ? NR : P)) {
-      const uint32_t a = smem_addr(&mb.sums[b][src][idx]);
+    if (lo_holder<S>(lane)) {
+      const uint32_t a = smem_addr(&mb.sums[b][src][lo_index<S>(lane)]);
 #pragma unroll
       for (int r = 0; r < sp.kc; ++r) st_async_f32(map_rank(a, r), tv, map_rank(bar, r));
     }
-    if constexpr (C::NR2 > 0) {
-      float hi[P2];
+    if (hi_holder<S>(lane)) {
+      const uint32_t a = smem_addr(&mb.sums[b][src][hi_index<S>(lane)]);
 #pragma unroll
-      for (int r = 0; r < P2; ++r) hi[r] = part[P + r];
-      const float tv2 = reduce_scatter<P2>(hi, lane);
-      const int idx2 = lane >> C::SHIFT2;
-      if ((lane & ((1 << C::SHIFT2) - 1)) == 0 && idx2 < C::NR2) {
-        const uint32_t a = smem_addr(&mb.sums[b][src][P + idx2]);
-#pragma unroll
-        for (int r = 0; r < sp.kc; ++r) st_async_f32(map_rank(a, r), tv2, map_rank(bar, r));
-      }
+      for (int r = 0; r < sp.kc; ++r) st_async_f32(map_rank(a, r), tv2, map_rank(bar, r));
     }
   }
 }
@@ -182,7 +293,6 @@ __device__ __forceinline__ void token_mix(Row row,
                                           AfterMix after_mix, const uint4 (&c)[VPT],
                                           f32x2 (&acc)[VPT][4], Split sp) {
   using C = TokenCfg<S, HAS_DELTA, HAS_ONORM, K, NW>;
-  constexpr int N = C::N;
   constexpr int NR = C::NR;
   if constexpr (S == 0) {
 #pragma unroll
@@ -198,40 +308,12 @@ __device__ __forceinline__ void token_mix(Row row,
 #pragma unroll 4
       for (int s = 0; s < sp.kc * NW; ++s) tot += mb.sums[b][s][lane];
     }
-    const float dtv = __shfl_sync(0xffffffffu, tot, (lane + N) & 31);
-    float logit = __int_as_float(0xff800000u);  // -inf
-    // reciprocal square root and a fast quotient (z in [1, N]): a few ulp of
-    // fp32 on the weights, far below the bf16 output's resolution, and the
-    // same instructions in every warp, so the weights stay bit-identical
-    if (lane < N) logit = dtv * rsqrtf(fmaf(tot, sp.inv_h, eps));
-    const float m = warp_max(logit);
-    const float e = (lane < N) ? expf(logit - m) : 0.f;
-    const float z = warp_sum(e);
-    const float wl = __fdividef(e, z);
-#pragma unroll
-    for (int v = 0; v < VPT; ++v)
-#pragma unroll
-      for (int k = 0; k < 4; ++k) acc[v][k] = 0ull;
-#pragma unroll
-    for (int i = 0; i < N; ++i) {
-      const float w = __shfl_sync(0xffffffffu, wl, i);
-      const f32x2 w2 = f2_make(w, w);
-#pragma unroll
-      for (int v = 0; v < VPT; ++v) {
-        const uint4 xi = (i < S) ? row(i < S ? i : 0, v) : c[v];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) acc[v][k] = f2_fma(w2, bf2_widen(vword(xi, k)), acc[v][k]);
-      }
-    }
+    const float wl = softmax_weight<S>(tot, lane, eps, sp.inv_h);
+    mix_rows<S, VPT>(row, c, wl, acc);
     after_mix();
   }
   if constexpr (HAS_ONORM) {
-    f32x2 sq2 = 0ull;
-#pragma unroll
-    for (int v = 0; v < VPT; ++v)
-#pragma unroll
-      for (int k = 0; k < 4; ++k) sq2 = f2_fma(acc[v][k], acc[v][k], sq2);
-    const float sq = warp_sum(f2_lo(sq2) + f2_hi(sq2));
+    const float sq = warp_sq<VPT>(acc);
     if (lane < sp.kc)
       st_async_f32(map_rank(smem_addr(&mb.sq[b][(int)rank * NW + warp]), lane), sq,
                    map_rank(smem_addr(&mb.bar_sq[b]), lane));
@@ -243,22 +325,13 @@ __device__ __forceinline__ void token_finish(typename TokenCfg<S, HAS_DELTA, HAS
                                              int b, uint32_t parity, int lane, float out_eps,
                                              bool& failed, unsigned* err, const uint4 (&ow)[VPT],
                                              f32x2 (&acc)[VPT][4], uint4 (&out)[VPT], Split sp) {
+  float ro = 1.f;
   if constexpr (HAS_ONORM) {
     wait_or_flag(smem_addr(&mb.bar_sq[b]), parity, failed, err, kErrExchangeTimeout);
     const float tot = warp_sum(lane < sp.kc * NW ? mb.sq[b][lane] : 0.f);
-    const float ro = rsqrtf(fmaf(tot, sp.inv_h, out_eps));
-    const f32x2 ro2 = f2_make(ro, ro);
-#pragma unroll
-    for (int v = 0; v < VPT; ++v)
-#pragma unroll
-      for (int k = 0; k < 4; ++k) acc[v][k] = f2_mul(f2_mul(acc[v][k], ro2), bf2_widen(vword(ow[v], k)));
+    ro = rsqrtf(fmaf(tot, sp.inv_h, out_eps));
   }
-#pragma unroll
-  for (int v = 0; v < VPT; ++v)
-    out[v] = make_uint4(pack_bf16x2(f2_lo(acc[v][0]), f2_hi(acc[v][0])),
-                        pack_bf16x2(f2_lo(acc[v][1]), f2_hi(acc[v][1])),
-                        pack_bf16x2(f2_lo(acc[v][2]), f2_hi(acc[v][2])),
-                        pack_bf16x2(f2_lo(acc[v][3]), f2_hi(acc[v][3])));
+  pack_out<HAS_ONORM, VPT>(acc, ow, ro, out);
 }
 
 // The three phases back to back (one token, no overlap); c must hold the

@@ -87,7 +87,8 @@ def make(name: str):
 # Sources the timed kernel (the stream kernel) is built from: a recorded
 # DRAM-traffic figure is used only while these are unchanged and for the same
 # kernel variant (template arguments).
-STREAM_SOURCES = ("attn_res_common.cuh", "attn_res_token.cuh", "attn_res_stream.cuh")
+STREAM_SOURCES = ("attn_res_common.cuh", "attn_res_token.cuh", "attn_res_stream.cuh",
+                  "attn_res_row.cuh")
 
 
 def source_digest() -> str:
@@ -107,14 +108,16 @@ def measured_peaks():
 
 
 def kernel_label(wl, shape) -> str:
-    """The timed kernel as ncu names it (template arguments of the launch)."""
+    """The timed kernel with its template arguments (S, delta, norm, split,
+    vectors per thread, ring depth, shared bank rows, staged)."""
     d, o = int(wl.delta is not None), int(wl.out_norm_w is not None)
-    if shape["kernel"] == "stream":
-        vpt = {(7, 32): 4, (7, 64): 2, (7, 128): 1, (4, 128): 2, (14, 32): 2, (14, 64): 1,
-               (2, 128): 4, (2, 64): 8}
-        v = vpt.get((shape["split"], shape["threads"]), 0)
+    if shape["kernel"] in ("stream", "staged"):
+        vpc = 896 // shape["split"]
+        v = -(-vpc // shape["threads"])  # vectors per thread
         return (f"attn_res_stream_kernel<{wl.num_blocks},{d},{o},{shape['split']},{v},"
-                f"{shape['stages']},{int(wl.group > 1)}>")
+                f"{shape['stages']},{int(wl.group > 1)},{int(shape['kernel'] == 'staged')}>")
+    if shape["kernel"] == "row":
+        return f"attn_res_row_kernel<{wl.num_blocks},{d},{o},{896 // shape['threads']}>"
     if shape["kernel"] == "split":
         return f"attn_res_split_kernel<{wl.num_blocks},{d},{o},{shape['split']}>"
     return f"attn_res_{shape['kernel']}_kernel<{wl.num_blocks},{d},{o}>"
@@ -213,7 +216,8 @@ class ClockSampler:
 
 def oracle_rate(wl, budget_s: float, threads: int):
     """Tokens/s of the oracle on a bounded sample of the workload: the first
-    n token rows, repeated passes until about budget_s of CPU time."""
+    n token rows, repeated passes until about budget_s of CPU time.  Also
+    returns the oracle's results for those rows (the first pass)."""
     import oracle
     n = min(wl.T, max(threads, 16))
     t0 = time.perf_counter()
@@ -221,14 +225,38 @@ def oracle_rate(wl, budget_s: float, threads: int):
     dt = time.perf_counter() - t0
     n = int(min(wl.T, max(n, n * budget_s / max(dt, 1e-6))))
     toks = np.arange(n)
-    passes, t0 = 0, time.perf_counter()
+    passes, t0, first = 0, time.perf_counter(), None
     while True:
-        oracle.run_workload(wl, n_threads=threads, tokens=toks)
+        r = oracle.run_workload(wl, n_threads=threads, tokens=toks)
+        first = first or r
         passes += 1
         dt = time.perf_counter() - t0
         if dt >= budget_s or passes >= 1000:
             break
-    return n * passes / dt, n, passes, dt
+    return n * passes / dt, n, passes, dt, first
+
+
+def widen(bits: np.ndarray) -> np.ndarray:
+    """bf16 bit patterns as float64 (exact)."""
+    return (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def compare_with_oracle(wl, gpu: dict, ref: dict) -> dict:
+    """The GPU's results for the oracle's token rows against the oracle: out
+    within max(2 bf16 ulp of the oracle value, 1e-2) per element, the
+    updated prefix and every bank slot of those rows bit-exact."""
+    idx = ref["tokens"]
+    g, r = widen(gpu["out"][idx]), widen(ref["out"])
+    ulp = np.exp2(np.floor(np.log2(np.maximum(np.abs(r), 2.0 ** -126))) - 7)
+    tol = np.maximum(2 * ulp, 1e-2)
+    ratio = np.abs(g - r) / tol
+    worst = float(np.max(ratio)) if ratio.size else 0.0
+    res = {"checked": True, "tokens": int(len(idx)), "max_err_over_tol": round(worst, 4),
+           "out_within_tol": bool(np.all(np.isfinite(g)) and worst <= 1.0),
+           "prefix_bitexact": bool(np.array_equal(gpu["prefix"][idx], ref["prefix"][:, :wl.H])),
+           "bank_bitexact": bool(np.array_equal(gpu["bank"][idx], ref["bank"]))}
+    res["ok"] = res["out_within_tol"] and res["prefix_bitexact"] and res["bank_bitexact"]
+    return res
 
 
 # ---- ranks --------------------------------------------------------------------
@@ -265,6 +293,18 @@ def call(ar, wl, t, stream, pdl=False):
                 t["out"], pdl=pdl, stream=stream, **TUNE)
 
 
+def warm_up(ar, wl, t, torch, stream, calls, min_seconds):
+    """At least `calls` calls and at least `min_seconds` of them, so the GPU
+    reaches its steady clocks and memory state whatever --warmup says."""
+    n, t0 = 0, time.perf_counter()
+    while n < calls or time.perf_counter() - t0 < min_seconds:
+        for _ in range(max(1, calls if n == 0 else 16)):
+            call(ar, wl, t, stream)
+            n += 1
+        torch.cuda.synchronize()
+    return n
+
+
 def time_device(ar, wl, t, torch, stream, steps, warmup):
     for _ in range(warmup):
         call(ar, wl, t, stream)
@@ -293,6 +333,29 @@ def input_sets(wl, t, torch, dev, at_least=1):
     return sets
 
 
+def replay_us(g, torch, stream, calls, warm_s=0.02, replays=5):
+    """µs per call of a captured graph of `calls` calls: replays for at least
+    `warm_s` seconds first (an idle GPU needs a moment to reach its steady
+    clocks), then the median of `replays` timed replays."""
+    t0 = time.perf_counter()
+    while True:
+        g.replay()
+        torch.cuda.synchronize()
+        if time.perf_counter() - t0 >= warm_s:
+            break
+    per = []
+    for _ in range(replays):
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            a.record(stream)
+            g.replay()
+            b.record(stream)
+        torch.cuda.synchronize()
+        per.append(a.elapsed_time(b) * 1e3 / calls)
+    return statistics.median(per)
+
+
 def time_graph(ar, wl, sets, torch, stream, calls=64, pdl=False):
     """Mean µs per call of `calls` back-to-back launches replayed from a CUDA
     graph (no host launch overhead), cycling through the input sets; with
@@ -304,17 +367,9 @@ def time_graph(ar, wl, sets, torch, stream, calls=64, pdl=False):
     with torch.cuda.graph(g, stream=stream):
         for i in range(calls):
             call(ar, wl, sets[i % len(sets)], stream, pdl=pdl)
-    g.replay()
-    torch.cuda.synchronize()
-    a = torch.cuda.Event(enable_timing=True)
-    b = torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        a.record(stream)
-        g.replay()
-        b.record(stream)
-    torch.cuda.synchronize()
+    us = replay_us(g, torch, stream, calls)
     del g
-    return a.elapsed_time(b) * 1e3 / calls
+    return us
 
 
 # every prefill case of the benchmark set: T x num_blocks x output norm x write-back
@@ -419,17 +474,8 @@ def tp_cells(ar, torch, dev, stream, peak, ranks=8):
             with torch.cuda.graph(g, stream=stream):
                 for i in range(calls):
                     step(sets[i % len(sets)])
-            g.replay()
-            torch.cuda.synchronize()
-            a = torch.cuda.Event(enable_timing=True)
-            b = torch.cuda.Event(enable_timing=True)
-            with torch.cuda.stream(stream):
-                a.record(stream)
-                g.replay()
-                b.record(stream)
-            torch.cuda.synchronize()
+            us = replay_us(g, torch, stream, calls)
             del g
-            us = a.elapsed_time(b) * 1e3 / calls
             gbs = alg / (us * 1e-6) / 1e9
             nch = -(-wl.T // chunk) if chunk else 1
             form = "single exchange (Gram)" if gram else "two exchanges"
@@ -448,6 +494,30 @@ def tp_cells(ar, torch, dev, stream, peak, ranks=8):
                          "frac_all_passes": round(moved / (us * 1e-6) / 1e9 / peak, 4),
                          "input_sets": len(sets)})
         del sets, shard
+        torch.cuda.empty_cache()
+    return rows
+
+
+DECODE = ["decode:64", "decode:256"]
+
+
+def decode_cells(ar, torch, dev, stream, peak):
+    """The decode-batch cells (T = 64 and 256, 8 bank rows, delta, output
+    norm): µs per call from graph replay over rotating input sets larger than
+    3x L2, without and with programmatic dependent launch."""
+    rows = []
+    for name in DECODE:
+        wl, _ = make(name)
+        t = device_tensors(wl, torch, dev)
+        sets = input_sets(wl, t, torch, dev, at_least=2)
+        us = time_graph(ar, wl, sets, torch, stream)
+        us_pdl = time_graph(ar, wl, sets, torch, stream, pdl=True)
+        gbs = wl.algorithmic_bytes() / (us * 1e-6) / 1e9
+        rows.append({"workload": name, "us_per_call": round(us, 2),
+                     "tokens_per_s": round(wl.T / (us * 1e-6), 1), "gbs": round(gbs, 1),
+                     "frac": round(gbs / peak, 4), "pdl_us_per_call": round(us_pdl, 2),
+                     "input_sets": len(sets)})
+        del t, sets
         torch.cuda.empty_cache()
     return rows
 
@@ -473,17 +543,7 @@ def pdl_chain(ar, torch, dev, stream):
             with torch.cuda.graph(g, stream=stream):
                 for i in range(n):
                     call(ar, wl, sets[i % len(sets)], stream, pdl=pdl)
-            g.replay()
-            torch.cuda.synchronize()
-            a = torch.cuda.Event(enable_timing=True)
-            b = torch.cuda.Event(enable_timing=True)
-            with torch.cuda.stream(stream):
-                a.record(stream)
-                for _ in range(4):
-                    g.replay()
-                b.record(stream)
-            torch.cuda.synchronize()
-            row["pdl_us_per_call" if pdl else "us_per_call"] = round(a.elapsed_time(b) * 1e3 / (4 * n), 3)
+            row["pdl_us_per_call" if pdl else "us_per_call"] = round(replay_us(g, torch, stream, n), 3)
             del g
         row["input_sets"] = len(sets)
         out[name] = row
@@ -519,20 +579,10 @@ def latency_t1(ar, torch, dev, stream, reps=200):
         with torch.cuda.graph(g, stream=stream):
             for _ in range(n):
                 call(ar, wl, t, stream)
-        g.replay()
-        torch.cuda.synchronize()
-        a = torch.cuda.Event(enable_timing=True)
-        b = torch.cuda.Event(enable_timing=True)
-        with torch.cuda.stream(stream):
-            a.record(stream)
-            for _ in range(5):
-                g.replay()
-            b.record(stream)
-        torch.cuda.synchronize()
         res[name] = {"flushed_p50": round(statistics.median(times), 3),
                      "flushed_p20": round(float(np.percentile(times, 20)), 3),
                      "flushed_p80": round(float(np.percentile(times, 80)), 3),
-                     "graph_per_call": round(a.elapsed_time(b) * 1e3 / (5 * n), 3)}
+                     "graph_per_call": round(replay_us(g, torch, stream, n), 3)}
         del t, g
     del flush
     return res
@@ -625,20 +675,52 @@ def run_ours(args, rank, world, local_rank, dist):
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
     wl, desc = make(args.workload)
-    t = device_tensors(wl, torch, dev)
     stream = torch.cuda.Stream(dev)
     TUNE.update(split=args.split, kernel=args.kernel, stages=args.stages, vpt=args.vpt)
     shape = ar.launch_shape(wl.T, wl.num_blocks, wl.out_norm_w is not None,
                             ar.FLAG_SPLIT(args.split) | ar.FLAG_KERNEL(args.kernel) |
-                            ar.FLAG_STAGES(args.stages) | ar.FLAG_VPT(args.vpt))
+                            ar.FLAG_STAGES(args.stages) | ar.FLAG_VPT(args.vpt),
+                            has_delta=wl.delta is not None)
 
-    for _ in range(max(args.warmup, 3)):
+    # The CPU-baseline leg (rank 0 of a one-GPU run), before the timed region:
+    # one call on fresh device buffers in the launch configuration that is
+    # timed, whose results for the oracle's sample rows must match the oracle
+    # (the run stops otherwise), and the oracle's own rate on that sample.
+    parity, cpu, cpu1 = None, None, None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        t = device_tensors(wl, torch, dev)
         call(ar, wl, t, stream)
-    torch.cuda.synchronize()
-    if dist is not None:
-        dist.barrier()
-    torch.cuda.synchronize()
+        torch.cuda.synchronize()
+        down = lambda x: x.cpu().view(torch.int16).numpy().view(np.uint16)
+        gpu = {"out": down(t["out"]), "prefix": down(t["prefix"]), "bank": down(t["bank"])}
+        del t
+        torch.cuda.empty_cache()
+        threads = os.cpu_count() or 1
+        rate, n, passes, dt, ref = oracle_rate(wl, args.cpu_budget, threads)
+        parity = compare_with_oracle(wl, gpu, ref)
+        parity["sample"] = f"first {n} token rows, one call on fresh buffers before timing"
+        del gpu, ref
+        cpu = {"value": round(rate, 2), "unit": "tokens/s", "cores": threads, "kind": "oracle",
+               "sample": f"first {n} token rows of the same workload, {passes} pass(es), {dt:.1f} s"}
+        rate1, n1, passes1, dt1, _ = oracle_rate(wl, args.cpu_budget / 2, 1)
+        cpu1 = {"value": round(rate1, 2), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                "sample": f"first {n1} token rows of the same workload, {passes1} pass(es), {dt1:.1f} s"}
+        if not parity["ok"]:
+            print(json.dumps({"metric": METRIC, "error": "GPU results differ from the oracle",
+                              "parity": parity}), flush=True)
+            sys.exit(3)
+
+    t = device_tensors(wl, torch, dev)
+    # the clock sampler starts first: its start-up pause must not fall between
+    # the warm-up and the timed region (an idle GPU drops its clocks, and the
+    # first timed launch then ran at 1.7x its steady time)
     with ClockSampler(local_rank) as clk:
+        w0 = time.perf_counter()
+        warm_calls = warm_up(ar, wl, t, torch, stream, max(args.warmup, 3), args.warmup_seconds)
+        warm_s = time.perf_counter() - w0
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
         w0 = time.time()
         total_ms, per = time_device(ar, wl, t, torch, stream, args.steps, 0)
         clk.mark(w0, time.time())
@@ -654,6 +736,7 @@ def run_ours(args, rank, world, local_rank, dist):
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "tokens/s",
         "n_gpus": world, "steps": args.steps, "warmup": max(args.warmup, 3),
+        "warmup_calls": warm_calls, "warmup_s": round(warm_s, 3),
         "ms_per_step": round(tmax / args.steps, 5), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "io_dtype": "bf16",
         "data": "synthetic (seeded numpy, distributions of the pages' workloads)",
@@ -671,8 +754,11 @@ def run_ours(args, rank, world, local_rank, dist):
                      "mean_launch_us": round(mean_launch_ms * 1e3, 3),
                      "launch_us_p20_p50_p80": [round(float(np.percentile(per, q)) * 1e3, 3)
                                                for q in (20, 50, 80)],
+                     "first_launches_us": [round(x * 1e3, 3) for x in per[:5]],
                      "traffic": recorded_traffic(args.workload, kernel_label(wl, shape)),
                      "kernel": kernel_label(wl, shape)},
+        "parity": parity if parity is not None else {"checked": False,
+                                                     "why": "one-GPU rank 0 with the CPU leg only"},
         "gpu_launches": args.steps,
         "clocks": clk.summary(),
         "device": device_info(torch, dev),
@@ -681,38 +767,51 @@ def run_ours(args, rank, world, local_rank, dist):
         line["latency_us"] = latency_t1(ar, torch, dev, stream)
     if rank == 0 and not args.no_latency:
         line["pdl_chain"] = pdl_chain(ar, torch, dev, stream)
+    del t
+    torch.cuda.empty_cache()
     if rank == 0 and not args.no_sweep:
-        del t
-        torch.cuda.empty_cache()
         line["prefill_cells"] = sweep_prefill(ar, torch, dev, stream, peak)
-        t = None
-    if rank == 0 and not args.no_sweep:
-        t = None
-        torch.cuda.empty_cache()
+        line["decode_cells"] = decode_cells(ar, torch, dev, stream, peak)
         line["width_cells"] = width_cells(ar, torch, dev, stream, peak)
     if rank == 0 and not args.no_tp:
-        t = None
-        torch.cuda.empty_cache()
         line["tp_cells"] = tp_cells(ar, torch, dev, stream, peak)
     if not args.no_e2e:
-        t = None
         torch.cuda.empty_cache()
         e = e2e(ar, wl, torch, dev, stream, max(3, min(args.steps, args.e2e_steps)))
         if dist is not None:
             e["ms_per_step"], e["value"] = combine_ranks(dist, e["ms_per_step"], wl.T, dev)
         e["value"] = round(e["value"], 1)
         line["e2e"] = e
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        threads = os.cpu_count() or 1
-        rate, n, passes, dt = oracle_rate(wl, args.cpu_budget, threads)
-        line["cpu_baseline"] = {"value": round(rate, 2), "unit": "tokens/s", "cores": threads,
-                                "kind": "oracle",
-                                "sample": f"first {n} token rows of the same workload, {passes} pass(es), {dt:.1f} s"}
-        rate1, n1, passes1, dt1 = oracle_rate(wl, args.cpu_budget / 2, 1)
-        line["cpu_baseline_one_core"] = {
-            "value": round(rate1, 2), "unit": "tokens/s", "cores": 1, "kind": "oracle",
-            "sample": f"first {n1} token rows of the same workload, {passes1} pass(es), {dt1:.1f} s"}
+    if cpu is not None:
+        line["cpu_baseline"] = cpu
+        line["cpu_baseline_one_core"] = cpu1
+    line["summary"] = summary(line, parity)
     return line
+
+
+def summary(line: dict, parity) -> dict:
+    """The figures the target is read from, last on the line: the parity
+    check, the timed kernel's fraction of the copy peak, the T = 1 latencies
+    (4 and 8 bank rows; L2 flushed before each call, p50, and back to back in
+    a graph), the worst prefill cell and the decode cells."""
+    out = {"parity_ok": None if parity is None else parity["ok"],
+           "parity_max_err_over_tol": None if parity is None else parity["max_err_over_tol"],
+           "parity_tokens": None if parity is None else parity["tokens"],
+           "headline_frac": line["roofline"]["frac"]}
+    lat = line.get("latency_us")
+    if lat:
+        out["t1_us"] = {k: {"flushed_p50": v["flushed_p50"], "graph": v["graph_per_call"]}
+                        for k, v in lat.items()}
+    cells = line.get("prefill_cells")
+    if cells:
+        worst = min(cells, key=lambda c: c["frac"])
+        out["prefill_min_frac"] = worst["frac"]
+        out["prefill_min_cell"] = worst["workload"]
+        out["prefill_cells_below_0.75"] = sum(c["frac"] < 0.75 for c in cells)
+    dec = line.get("decode_cells")
+    if dec:
+        out["decode_us"] = {c["workload"]: c["us_per_call"] for c in dec}
+    return out
 
 
 def run_reference(args, rank, world):
@@ -756,6 +855,8 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--warmup-seconds", type=float, default=0.3,
+                    help="warm up for at least this long, whatever --warmup says")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="long_prefill")
     ap.add_argument("--split", type=int, default=0, help="CTAs per token row (0 = automatic)")

@@ -71,22 +71,48 @@ typedef enum {
 
 /* Tuning overrides (0 = automatic).  Results do not depend on them beyond
  * fp32 summation order.
- *   SPLIT(k):  CTAs (one thread-block cluster) a token row is split over;
- *              split kernel 4, 7, 8, 14 or 16; stream kernel see below.
  *   KERNEL(k): ATTN_RES_KERNEL_SPLIT -- one cluster per token row, rows held
  *              in registers (latency path for few tokens);
  *              ATTN_RES_KERNEL_STREAM -- persistent clusters that stream many
- *              tokens through a TMA-filled shared-memory ring.
- *   STAGES(n): ring depth of the stream kernel.
- *   VPT(n):    16-byte vectors per thread and row (split kernel: 1).
+ *              tokens through a TMA-filled shared-memory ring of bank rows,
+ *              prefix and delta loaded into registers one token ahead;
+ *              ATTN_RES_KERNEL_STAGED -- the stream kernel with prefix and
+ *              delta also in the ring, as deep as shared memory allows;
+ *              ATTN_RES_KERNEL_ROW -- one CTA per token row holding the whole
+ *              row in registers, no cluster (up to 2 bank rows);
+ *              ATTN_RES_KERNEL_ROW_SMEM -- the same with the rows in shared
+ *              memory, brought in by bulk copies (1..5 bank rows).
+ *   SPLIT(k):  CTAs (one thread-block cluster) a token row is split over;
+ *              split kernel 4, 7, 8, 14 or 16; stream kernel see below; the
+ *              row kernels 1.
+ *   STAGES(n): ring depth of the stream kernel; CTAs per SM the staged
+ *              form's ring is sized for.
+ *   VPT(n):    16-byte vectors per thread and row (split kernel: 1; row
+ *              kernels: 4 or 7).
  * Stream kernel shapes (split, vpt, stages): (7,1,2) (7,2,2) (7,2,3) (7,4,2)
  * (4,2,2) (4,2,3) (2,4,2) (14,2,2) (2,8,2).  Unset fields default to:
  * split 2 with no bank rows (4 if VPT 2 is given, 7 for VPT 1), else 7;
  * stages 2; VPT 8 with split 2 and no bank rows, 4 with split 2 and bank
  * rows or with split 7, 1..5 bank rows and an output norm, else 2 -- so
  * (7,4,2), (2,8,2) with no bank rows, and (7,2,2) otherwise.
- * The kernel defaults to the split kernel below 80 tokens and when there is
- * neither a bank row nor an output norm, else the stream kernel. */
+ * Staged shapes (split, vpt, CTAs per SM): (4,4,5) (7,4,7) (4,4,4); the
+ * ring holds as many stages of the S + 1 (+1 with delta) row slices as fit,
+ * and a shape whose ring cannot hold two is ATTN_RES_EINVAL for that S.
+ * Without overrides: (4,4,5) for 3 bank rows, (7,4,7) for 4, (4,4,4) for 5.
+ * Automatic choice (shape overrides without KERNEL keep to the split and
+ * stream kernels), measured per case on GB300:
+ *   T < 80, or shared bank rows below 80: the split kernel;
+ *   shared bank rows (B > 1) from 80 rows: the stream kernel;
+ *   otherwise, with an output norm: no bank row, the row kernel; 1 bank row,
+ *   the row kernel below 512 rows and the shared-memory row kernel from
+ *   512; 2, the row kernel below 4096 rows and the shared-memory one from
+ *   4096; 3..5, the shared-memory row kernel below 512 rows and the staged
+ *   form from 512; 6..8, the stream kernel;
+ *   without an output norm, below 512 rows: no bank row, the split kernel;
+ *   1..2, the row kernel; 3, the staged form; 4..5, the shared-memory row
+ *   kernel; 6..8, the stream kernel; from 512 rows: 0..1 bank rows, the row
+ *   kernel, else the stream kernel.
+ * (The exact table is attn_res_launch_shape's answer.) */
 #define ATTN_RES_FLAG_SPLIT(k) (((uint32_t)(k) & 0xffu) << 8)
 #define ATTN_RES_FLAG_KERNEL(k) (((uint32_t)(k) & 0xfu) << 16)
 #define ATTN_RES_FLAG_STAGES(n) (((uint32_t)(n) & 0xfu) << 20)
@@ -94,6 +120,9 @@ typedef enum {
 #define ATTN_RES_KERNEL_SPLIT 1
 #define ATTN_RES_KERNEL_STREAM 2
 #define ATTN_RES_KERNEL_GENERIC 3 /* one CTA per row, any H (see attn_res_h) */
+#define ATTN_RES_KERNEL_STAGED 4  /* stream kernel with prefix and delta staged in the ring */
+#define ATTN_RES_KERNEL_ROW 5     /* one CTA per token row, the whole row */
+#define ATTN_RES_KERNEL_ROW_SMEM 6 /* the same with the rows in shared memory */
 
 /* Memory layout of the tensors, in elements.  A row is H contiguous
  * elements; columns H .. stride-1 are padding that is never read or
@@ -184,7 +213,9 @@ attn_res_status_t attn_res(attn_res_bf16_t* prefix, const attn_res_bf16_t* delta
  *     arithmetic, the rows read three times through L2), a functional
  *     path.  ATTN_RES_FLAG_KERNEL(ATTN_RES_KERNEL_GENERIC) forces it, also at
  *     H == ATTN_RES_HIDDEN.  Forcing a fast kernel where no form of it fits
- *     the width (or the row has no exchange) is ATTN_RES_EINVAL.
+ *     the width (or the row has no exchange) is ATTN_RES_EINVAL; the row
+ *     kernels and the staged form are built for H == ATTN_RES_HIDDEN only
+ *     (forced at another width: ATTN_RES_EINVAL).
  * Returns ATTN_RES_EINVAL for a bad H.  (No counterpart on the pages, whose
  * kernel is built for H = 7168 only.)
  */
@@ -289,16 +320,19 @@ int attn_res_max_blocks(void);
 
 /*
  * attn_res_launch_shape -- the launch attn_res would make for T rows with
- * num_blocks sources, output norm on/off and the given flags: the kernel
- * (ATTN_RES_KERNEL_*), CTAs per token row (`split`), ring depth (`stages`, 0
- * for the split kernel), threads per CTA, CTAs in the grid (0 for the stream
- * kernel, whose grid is as many clusters as fit on the device, at most T) and
- * the thread-block cluster size (1 when the CTAs of a row never exchange
- * sums: no bank rows and no output norm).  Any output pointer may be NULL.
- * Pure host computation, no CUDA call.  Returns ATTN_RES_EINVAL for T < 0,
- * num_blocks outside 0..8 or an unsupported override.
+ * num_blocks sources, a delta row or not, output norm on/off and the given
+ * flags: the kernel (ATTN_RES_KERNEL_*), CTAs per token row (`split`), ring
+ * depth (`stages`: the stream kernel's STAGES; the staged form's depth,
+ * which follows from the rows of a stage; 0 for the other kernels), threads
+ * per CTA, CTAs in the grid (0 for the persistent stream kernel and its
+ * staged form, whose grid is as many clusters as fit on the device, at most
+ * T) and the thread-block cluster size (1 when the CTAs of a row never
+ * exchange sums -- no bank rows and no output norm -- and for the row and
+ * general kernels, which hold a row in one CTA).  Any output pointer may be
+ * NULL.  Pure host computation, no CUDA call.  Returns ATTN_RES_EINVAL for
+ * T < 0, num_blocks outside 0..8 or an unsupported override.
  */
-attn_res_status_t attn_res_launch_shape(int64_t T, int num_blocks,
+attn_res_status_t attn_res_launch_shape(int64_t T, int num_blocks, int has_delta,
                                         int has_out_norm, uint32_t flags,
                                         int* kernel, int* split, int* stages,
                                         int* threads_per_cta, int64_t* ctas,

@@ -46,9 +46,25 @@ def test_launch_shape(lib):
     assert ls(1, 4, True) == dict(kernel="split", split=7, stages=0, threads=128, ctas=7, cluster=7)
     assert ls(64, 8, False) == dict(kernel="split", split=7, stages=0, threads=128, ctas=448, cluster=7)
     assert ls(8192, 8, True) == dict(kernel="stream", split=7, stages=2, threads=64, ctas=0, cluster=7)
-    assert ls(8192, 4, True) == dict(kernel="stream", split=7, stages=2, threads=32, ctas=0, cluster=7)
+    # 4 bank rows, output norm, many tokens: the staged form (7,4) at 7 CTAs
+    # per SM, two stages of 6 row slices with delta, three of 5 without
+    assert ls(8192, 4, True) == dict(kernel="staged", split=7, stages=2, threads=32, ctas=0, cluster=7)
+    assert ls(8192, 4, True, has_delta=False)["stages"] == 3
+    assert ls(256, 4, True) == dict(kernel="row_smem", split=1, stages=0, threads=128, ctas=256, cluster=1)
+    assert ls(256, 4, True, ar.FLAG_KERNEL(2)) == dict(kernel="stream", split=7, stages=2, threads=32, ctas=0, cluster=7)
     assert ls(8192, 4, False) == dict(kernel="stream", split=7, stages=2, threads=64, ctas=0, cluster=7)
-    assert ls(8192, 0, True) == dict(kernel="stream", split=2, stages=2, threads=64, ctas=0, cluster=2)
+    assert ls(2048, 3, True)["kernel"] == "staged" and ls(2048, 5, True)["kernel"] == "staged"
+    assert ls(256, 3, False) == dict(kernel="staged", split=4, stages=2, threads=64, ctas=0, cluster=4)
+    assert ls(2048, 6, True)["kernel"] == "stream"
+    # up to two bank rows: the row kernel, one CTA of 896 / VPT threads per row
+    assert ls(8192, 0, True) == dict(kernel="row", split=1, stages=0, threads=128, ctas=8192, cluster=1)
+    assert ls(256, 0, True)["threads"] == 224 and ls(256, 1, False)["threads"] == 224
+    assert ls(2048, 1, True)["kernel"] == "row_smem" and ls(2048, 2, True)["kernel"] == "row"
+    assert ls(4096, 2, True)["kernel"] == "row_smem" and ls(2048, 2, True)["threads"] == 128
+    assert ls(2048, 2, False)["kernel"] == "stream" and ls(256, 0, False)["kernel"] == "split"
+    assert ls(300, 2, True, ar.FLAG_KERNEL(5) | ar.FLAG_VPT(4))["threads"] == 224
+    # shape overrides without a kernel keep the split / stream families
+    assert ls(8192, 0, True, ar.FLAG_STAGES(2))["kernel"] == "stream"
     assert ls(8192, 0, True, ar.FLAG_VPT(4)) == dict(kernel="stream", split=2, stages=2, threads=128, ctas=0, cluster=2)
     assert ls(8192, 4, True, ar.FLAG_SPLIT(2))["threads"] == 128      # (2,4,2) with bank rows
     assert ls(8192, 0, True, ar.FLAG_VPT(2))["split"] == 4
@@ -58,7 +74,7 @@ def test_launch_shape(lib):
         ls(8192, 0, True, ar.FLAG_STAGES(3))          # (2,4,3) is not built
     assert ls(9000, 0, True, ar.FLAG_SPLIT(2))["threads"] == 64
     # no softmax and no output norm: the CTAs of a token never talk
-    assert ls(1024, 0, False) == dict(kernel="split", split=7, stages=0, threads=128, ctas=7168, cluster=1)
+    assert ls(256, 0, False) == dict(kernel="split", split=7, stages=0, threads=128, ctas=1792, cluster=1)
     assert ls(2, 8, True, ar.FLAG_SPLIT(16)) == dict(kernel="split", split=16, stages=0, threads=64, ctas=32, cluster=16)
     assert ls(2, 8, True, ar.FLAG_SPLIT(4))["threads"] == 224
     assert ls(2, 8, True, ar.FLAG_SPLIT(14))["threads"] == 64
@@ -68,7 +84,13 @@ def test_launch_shape(lib):
     assert ls(9000, 8, True, ar.FLAG_SPLIT(7) | ar.FLAG_VPT(2))["threads"] == 64
     assert ls(9000, 8, True, ar.FLAG_SPLIT(7) | ar.FLAG_VPT(1))["threads"] == 128
     for bad in [(-1, 0, 0, 0), (1, 9, 0, 0), (1, -1, 0, 0), (1, 1, 0, ar.FLAG_SPLIT(5)),
-                (1, 1, 0, ar.FLAG_KERNEL(4)), (1, 1, 0, ar.FLAG_KERNEL(2) | ar.FLAG_SPLIT(16)),
+                (1, 1, 0, ar.FLAG_KERNEL(7)), (1, 1, 0, ar.FLAG_KERNEL(2) | ar.FLAG_SPLIT(16)),
+                (1, 3, 0, ar.FLAG_KERNEL(5)), (1, 0, 0, ar.FLAG_KERNEL(5) | ar.FLAG_VPT(2)),
+                (1, 0, 0, ar.FLAG_KERNEL(5) | ar.FLAG_SPLIT(2)),
+                (1, 0, 0, ar.FLAG_KERNEL(6)), (1, 6, 0, ar.FLAG_KERNEL(6)),
+                (1, 3, 0, ar.FLAG_KERNEL(6) | ar.FLAG_VPT(1)),
+                (1, 8, 0, ar.FLAG_KERNEL(4)),
+                (1, 2, 0, ar.FLAG_KERNEL(4) | ar.FLAG_SPLIT(7) | ar.FLAG_VPT(2) | ar.FLAG_STAGES(2)),
                 (1, 1, 0, ar.FLAG_KERNEL(3) | ar.FLAG_SPLIT(7)),
                 (1, 1, 0, ar.FLAG_KERNEL(2) | ar.FLAG_STAGES(4)),
                 (1, 1, 0, ar.FLAG_KERNEL(2) | ar.FLAG_SPLIT(8) | ar.FLAG_VPT(2)),

@@ -205,6 +205,97 @@ def test_stream_kernel(S, shape):
                kernel=ar.KERNEL_STREAM, split=k, vpt=v, stages=st)
 
 
+# staged shapes: (split, vectors per thread, CTAs per SM); the ring depth is
+# what fits in shared memory for the stage's rows (bank rows, prefix, delta)
+STAGED = [(4, 4, 5), (7, 4, 7), (4, 4, 4)]
+STAGED_CASES = [(S, sh) for S in range(9) for sh in STAGED]
+
+
+def staged_depth(S, has_delta, shape):
+    """Ring depth of a staged shape: stages of (S + 1 + delta) row slices of
+    14336 / split bytes in an SM's 228 KB shared by `ctas_per_sm` CTAs, each
+    also holding its mailboxes, 8 stage barrier pairs and 1 KB of system
+    reserve, within 227 KB per CTA; at most 8 stages."""
+    k, v, cps = shape
+    nw = (896 // k // v + 31) // 32
+    static = 2 * k * nw * 2 * (S + 1) * 4 + 2 * k * nw * 4 + 32 + 16 * 8
+    budget = min(233472 // cps - 1024 - static, 232448 - static)
+    return min(8, budget // ((S + (2 if has_delta else 1)) * (14336 // k)))
+
+
+@pytest.mark.parametrize("S,shape", STAGED_CASES,
+                         ids=[f"S{S}_k{k}_v{v}_c{c}" for S, (k, v, c) in STAGED_CASES])
+def test_staged_kernel(S, shape):
+    """Every num_blocks x staged shape: 2500 tokens, so each CTA reuses
+    every stage of even the deepest ring; shapes whose ring cannot hold two
+    stages of the rows are refused."""
+    k, v, c = shape
+    i = S * len(STAGED) + STAGED.index(shape)
+    d, o = bool(i & 1), bool(i & 2)
+    w = [-1, S, 8][i % 3]
+    wl = W.make_workload(2500, S, capacity=9, has_delta=d, has_out_norm=o,
+                         block_write_idx=w, seed=100 + i, mixing=True,
+                         slot_stride=7168 + 8 * (i % 2))
+    if staged_depth(S, d, shape) < 2:
+        with pytest.raises(ar.AttnResError) as e:
+            G.run_gpu(wl, kernel=ar.KERNEL_STAGED, split=k, vpt=v, stages=c)
+        assert e.value.status == 1
+        return
+    full_check(wl, tag=f"staged_S{S}_k{k}_v{v}_c{c}_d{int(d)}_o{int(o)}_w{w}",
+               kernel=ar.KERNEL_STAGED, split=k, vpt=v, stages=c)
+
+
+# ---- the row kernel (one CTA per token row) ----------------------------------------
+
+ROW_VPTS = (4, 7)
+ROW_CASES = [(S, v, d, o) for S in range(3) for v in ROW_VPTS for d in (False, True)
+             for o in (False, True)]
+
+
+@pytest.mark.parametrize("S,vpt,d,o", ROW_CASES,
+                         ids=[f"S{S}_v{v}_d{int(d)}_o{int(o)}" for S, v, d, o in ROW_CASES])
+def test_row_kernel(S, vpt, d, o):
+    """Every num_blocks x vectors per thread x delta x output norm of the row
+    kernel, with the write-back slot (a source, the append slot or none) and
+    padded bank slots varying by case."""
+    i = ROW_CASES.index((S, vpt, d, o))
+    w = [-1, S, 8][i % 3]
+    wl = W.make_workload(300, S, capacity=9, has_delta=d, has_out_norm=o,
+                         block_write_idx=w, seed=200 + i, mixing=True,
+                         slot_stride=7168 + 8 * (i % 2))
+    full_check(wl, tag=f"row_S{S}_v{vpt}_d{int(d)}_o{int(o)}_w{w}", kernel=ar.KERNEL_ROW, vpt=vpt)
+
+
+ROW_SMEM_CASES = [(S, v, d, o) for S in range(1, 6) for v in ROW_VPTS for d in (False, True)
+                  for o in (False, True)]
+
+
+@pytest.mark.parametrize("S,vpt,d,o", ROW_SMEM_CASES,
+                         ids=[f"S{S}_v{v}_d{int(d)}_o{int(o)}" for S, v, d, o in ROW_SMEM_CASES])
+def test_row_smem_kernel(S, vpt, d, o):
+    """The row kernel with its rows in shared memory: 1..5 bank rows x
+    vectors per thread x delta x output norm, write-back slot and padded
+    bank slots varying by case."""
+    i = ROW_SMEM_CASES.index((S, vpt, d, o))
+    w = [-1, S, 8][i % 3]
+    wl = W.make_workload(300, S, capacity=9, has_delta=d, has_out_norm=o,
+                         block_write_idx=w, seed=300 + i, mixing=True,
+                         slot_stride=7168 + 8 * (i % 2))
+    full_check(wl, tag=f"row_smem_S{S}_v{vpt}_d{int(d)}_o{int(o)}_w{w}",
+               kernel=ar.KERNEL_ROW_SMEM, vpt=vpt)
+
+
+@pytest.mark.parametrize("S,vpt", [(3, 7), (8, 4), (0, 2), (1, 1)])
+def test_row_kernel_refuses_unbuilt_shapes(S, vpt):
+    """The row kernel is built for up to two bank rows and 4 or 7 vectors per
+    thread; anything else is refused before a launch."""
+    wl = W.make_workload(4, S, capacity=9, has_delta=True, has_out_norm=True,
+                         block_write_idx=-1, seed=3)
+    with pytest.raises(ar.AttnResError) as e:
+        G.run_gpu(wl, kernel=ar.KERNEL_ROW, vpt=vpt)
+    assert e.value.status == 1
+
+
 @pytest.mark.parametrize("T", [1, 2, 7, 1500])
 def test_stream_kernel_token_counts(T):
     """Fewer tokens than clusters, and many tokens per cluster."""
@@ -223,7 +314,7 @@ def test_zz_device_status_clean():
     assert ar.device_status() == 0
 
 
-@pytest.mark.parametrize("kernel", [ar.KERNEL_SPLIT, ar.KERNEL_STREAM])
+@pytest.mark.parametrize("kernel", [ar.KERNEL_SPLIT, ar.KERNEL_STREAM, ar.KERNEL_ROW])
 def test_subnormal_current_row_is_correctly_rounded(kernel):
     """c = bf16_rn(prefix + delta) must keep bf16 subnormals (no flush to
     zero) and round ties to even, in both kernels: prefix and delta drawn
@@ -310,7 +401,11 @@ def test_generic_kernel_forced_at_full_width(S):
 # writes it), and the rejection of a written source slot.
 GROUPED = [(B, T, S, w, k) for B in (2, 3, 8) for (T, S, w) in ((5, 4, -1), (37, 8, 8), (300, 8, 8),
                                                                  (300, 0, 2), (37, 1, 5))
-           for k in (ar.KERNEL_SPLIT, ar.KERNEL_STREAM, ar.KERNEL_GENERIC)]
+           for k in (ar.KERNEL_SPLIT, ar.KERNEL_STREAM, ar.KERNEL_GENERIC, ar.KERNEL_ROW,
+                     ar.KERNEL_ROW_SMEM)
+           # the row kernels are built for up to two (registers) and 1..5 bank
+           # rows (shared memory)
+           if (k != ar.KERNEL_ROW or S <= 2) and (k != ar.KERNEL_ROW_SMEM or 1 <= S <= 5)]
 
 
 @pytest.mark.parametrize("B,T,S,w,kernel", GROUPED,
@@ -336,7 +431,8 @@ def _nan_equal(a, b):
     return bool(np.all((a == b) | both_nan))
 
 
-@pytest.mark.parametrize("kernel", [ar.KERNEL_SPLIT, ar.KERNEL_STREAM, ar.KERNEL_GENERIC])
+@pytest.mark.parametrize("kernel", [ar.KERNEL_SPLIT, ar.KERNEL_STREAM, ar.KERNEL_GENERIC,
+                                    ar.KERNEL_ROW])
 def test_nonfinite_inputs_stay_in_their_token(kernel):
     """A NaN or an infinity in one token's rows makes that token's output NaN
     (IEEE arithmetic, as in the oracle) and leaves every other token as the
