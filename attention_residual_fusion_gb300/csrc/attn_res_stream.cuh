@@ -357,11 +357,13 @@ __device__ __forceinline__ void stream_body(const Params& p, const int64_t T) {
   // of taking SM slots from clusters still streaming.
   grid_dep_launch_dependents();
 
-  // After a time-out, do not leave with copies still landing in shared memory.
-  if (tid == 0 && failed) {
+  // After a time-out anywhere in the CTA, do not leave with copies or a
+  // peer's partial sums still landing in shared memory.
+  if (__syncthreads_or(failed) && tid == 0) {
     for (int s = 0; s < STAGES; ++s)
       if (pending & (1u << s))
         (void)mbar_wait_bounded(smem_addr(&full_bar[s]), (pending_parity >> s) & 1u);
+    if (COMM) mailbox_drain<Tok>(mb, ntok - 1, HAS_ONORM);
   }
 }
 

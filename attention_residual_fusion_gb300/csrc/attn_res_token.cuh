@@ -97,6 +97,20 @@ __device__ __forceinline__ void mailbox_expect(typename Cfg::Box& mb, int b, boo
   if (has_onorm) mbar_arrive_expect_tx(smem_addr(&mb.bar_sq[b]), senders * 4u);
 }
 
+// Time-out path only (thread 0, at exit): wait, bounded, for the last phase
+// armed on each mailbox buffer -- token `last` and the one before it -- so
+// that no peer's partial sums still land in this CTA's shared memory after it
+// exits.  A phase that already completed returns at once.
+template <class Cfg>
+__device__ __forceinline__ void mailbox_drain(typename Cfg::Box& mb, int64_t last, bool has_onorm) {
+  for (int64_t j = last; j >= 0 && j >= last - 1; --j) {
+    const int b = (int)(j & 1);
+    const uint32_t parity = (uint32_t)((j >> 1) & 1);
+    if (Cfg::N > 1) (void)mbar_wait_bounded(smem_addr(&mb.bar_sums[b]), parity);
+    if (has_onorm) (void)mbar_wait_bounded(smem_addr(&mb.bar_sq[b]), parity);
+  }
+}
+
 // q = rms_w * res_w for the thread's columns, as fp32 pairs.
 template <int VPT>
 __device__ __forceinline__ void make_query(const uint4 (&rw)[VPT], const uint4 (&qw)[VPT],

@@ -305,12 +305,19 @@ def warm_up(ar, wl, t, torch, stream, calls, min_seconds):
     return n
 
 
-def time_device(ar, wl, t, torch, stream, steps, warmup):
+def time_device(ar, wl, t, torch, stream, steps, warmup, ev=None):
+    """Device time of `steps` back-to-back calls (CUDA events on the launching
+    stream).  `ev`: the steps + 1 events, created beforehand so that nothing
+    slow runs between the synchronize before the region and its first call."""
+    ev = ev or [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
     for _ in range(warmup):
         call(ar, wl, t, stream)
     torch.cuda.synchronize()
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
     with torch.cuda.stream(stream):
+        # a ~0.1 ms device-side pause ahead of the region, so the host has
+        # queued the first calls when it starts: the first timed call then
+        # measures the device, not the host's launch latency (untimed)
+        torch.cuda._sleep(200_000)
         ev[0].record(stream)
         for i in range(steps):
             call(ar, wl, t, stream)
@@ -714,6 +721,7 @@ def run_ours(args, rank, world, local_rank, dist):
     # the clock sampler starts first: its start-up pause must not fall between
     # the warm-up and the timed region (an idle GPU drops its clocks, and the
     # first timed launch then ran at 1.7x its steady time)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
     with ClockSampler(local_rank) as clk:
         w0 = time.perf_counter()
         warm_calls = warm_up(ar, wl, t, torch, stream, max(args.warmup, 3), args.warmup_seconds)
@@ -722,7 +730,7 @@ def run_ours(args, rank, world, local_rank, dist):
             dist.barrier()
         torch.cuda.synchronize()
         w0 = time.time()
-        total_ms, per = time_device(ar, wl, t, torch, stream, args.steps, 0)
+        total_ms, per = time_device(ar, wl, t, torch, stream, args.steps, 0, ev)
         clk.mark(w0, time.time())
     if dist is not None:
         dist.barrier()

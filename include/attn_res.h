@@ -60,9 +60,18 @@ typedef enum {
  * kernel of the stream is still running.  It loads the bank rows and the
  * weights first, then waits for that kernel (griddepcontrol.wait) before
  * reading prefix and delta, and lets its own dependents launch once those
- * loads are issued.  Contract: the bank rows read and the weights must not be
- * written by the immediately preceding kernel of the stream.  Placement of
- * the wait: PDL discipline in the key source excerpts of vllm PR #54261. */
+ * loads are issued (the stream kernel and its staged form: once it has run
+ * out of tokens).  Contract: no grid that may still be running when this
+ * call's grid starts may write the bank rows it reads or the weights.  That
+ * is the preceding kernel of the stream, and also any earlier one that the
+ * preceding kernel lets run on -- a kernel that releases its dependents
+ * before its own grid-dependency wait.  The kernels here wait before they
+ * release, so in a chain of these calls only the immediately preceding
+ * call counts: between a call that writes a bank slot and a later PDL call
+ * that reads it, put a kernel launched without PDL (or any fully
+ * stream-ordered operation), or make the reading call without the flag.
+ * Placement of the wait: PDL discipline in the key source excerpts of vllm
+ * PR #54261. */
 #define ATTN_RES_FLAG_PDL 0x1u
 
 /* Hidden-sharded calls only (attn_res_tp_*; attn_res and attn_res_h reject

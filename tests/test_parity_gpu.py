@@ -372,6 +372,55 @@ def test_pdl_chain_in_graph(T):
 
 
 
+@pytest.mark.parametrize("T", [1, 300, 1024])
+def test_pdl_chain_with_bank_writes_in_graph(T):
+    """A chain captured in a CUDA graph in which one call writes a bank slot
+    that a later call reads as a source: call 1 (PDL) appends c to slot 2, a
+    plain kernel launched without PDL follows, then call 2 (PDL) mixes slots
+    0..2 and the prefix call 1 updated.  Call 2 reads its bank rows before
+    its grid-dependency wait, so the plain kernel between them is what the
+    PDL contract asks for (no grid that may still be running when a PDL call
+    starts writes the rows it reads).  Equal to the oracle applied twice in
+    sequence.  Two bank rows then three: the row, shared-memory row and
+    staged kernels at 300 and 1024 rows, the split kernel at one."""
+    import torch
+    wl1 = W.make_workload(T, 2, capacity=8, has_delta=True, has_out_norm=True,
+                          block_write_idx=2, seed=50 + T, mixing=True)
+    r1 = oracle.run_workload(wl1, n_threads=NT)
+    wl2 = wl1.copy()
+    wl2.prefix, wl2.bank = r1["prefix"], r1["bank"]
+    wl2.num_blocks, wl2.block_write_idx = 3, -1
+    wl2.delta = W.make_workload(T, 0, capacity=1, has_delta=True, has_out_norm=False,
+                                block_write_idx=-1, seed=90 + T).delta
+    r2 = oracle.run_workload(wl2, n_threads=NT)
+    up = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).cuda().view(torch.bfloat16)
+    down = lambda t: t.cpu().view(torch.int16).numpy().view(np.uint16)
+    d = dict(prefix=up(wl1.prefix), d1=up(wl1.delta), d2=up(wl2.delta), bank=up(wl1.bank),
+             rms=up(wl1.rms_w), res=up(wl1.res_w), onw=up(wl1.out_norm_w))
+    out1, out2 = torch.empty_like(d["prefix"]), torch.empty_like(d["prefix"])
+    pad = torch.zeros(1 << 16, device="cuda")
+    s = torch.cuda.Stream()
+    a1 = (d["prefix"], d["d1"], d["bank"], 2, 2, d["res"], d["rms"], d["onw"], 1e-6, 1e-6, out1)
+    a2 = (d["prefix"], d["d2"], d["bank"], 3, -1, d["res"], d["rms"], d["onw"], 1e-6, 1e-6, out2)
+    ar.attn_res(*a1, pdl=True, stream=s)   # one-time set-up outside capture
+    ar.attn_res(*a2, pdl=True, stream=s)
+    torch.cuda.synchronize()
+    d["prefix"].copy_(up(wl1.prefix))
+    d["bank"].copy_(up(wl1.bank))
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        ar.attn_res(*a1, pdl=True, stream=s)
+        pad.add_(1.0)                        # a kernel launched without PDL
+        ar.attn_res(*a2, pdl=True, stream=s)
+    g.replay()
+    torch.cuda.synchronize()
+    assert np.array_equal(down(d["prefix"]), r2["prefix"])
+    assert np.array_equal(down(d["bank"]), r2["bank"])
+    G.assert_out_close(down(out1), r1["out"], "pdl-write-chain call 1")
+    G.assert_out_close(down(out2), r2["out"], "pdl-write-chain call 2")
+
+
 # ---- the general kernel (any H, multiple of 8) -----------------------------------
 
 GEN = [(H, S) for H in (8, 16, 64, 200, 1024, 4096) for S in (0, 1, 3, 8)]
@@ -431,17 +480,23 @@ def _nan_equal(a, b):
     return bool(np.all((a == b) | both_nan))
 
 
-@pytest.mark.parametrize("kernel", [ar.KERNEL_SPLIT, ar.KERNEL_STREAM, ar.KERNEL_GENERIC,
-                                    ar.KERNEL_ROW])
-def test_nonfinite_inputs_stay_in_their_token(kernel):
+# (kernel, bank rows it is built for, the two bank slots that get a NaN and an
+# infinity)
+NONFINITE = [(ar.KERNEL_SPLIT, 8, 2, 5), (ar.KERNEL_STREAM, 8, 2, 5), (ar.KERNEL_GENERIC, 8, 2, 5),
+             (ar.KERNEL_ROW, 2, 1, 0), (ar.KERNEL_ROW_SMEM, 5, 2, 4), (ar.KERNEL_STAGED, 4, 2, 3)]
+
+
+@pytest.mark.parametrize("kernel,S,nan_slot,inf_slot", NONFINITE,
+                         ids=[f"k{k}_S{S}" for k, S, _, _ in NONFINITE])
+def test_nonfinite_inputs_stay_in_their_token(kernel, S, nan_slot, inf_slot):
     """A NaN or an infinity in one token's rows makes that token's output NaN
     (IEEE arithmetic, as in the oracle) and leaves every other token as the
     oracle computes it; write-backs stay exact (NaN for NaN)."""
-    wl = W.make_workload(37, 8, capacity=9, has_delta=True, has_out_norm=True,
+    wl = W.make_workload(37, S, capacity=9, has_delta=True, has_out_norm=True,
                          block_write_idx=8, seed=44, mixing=True)
     nan, inf = np.uint16(0x7FC0), np.uint16(0x7F80)
-    wl.bank[3, 2, 100] = nan          # a bank row of token 3
-    wl.bank[7, 5, 50] = inf           # an infinite bank element of token 7
+    wl.bank[3, nan_slot, 100] = nan   # a bank row of token 3
+    wl.bank[7, inf_slot, 50] = inf    # an infinite bank element of token 7
     wl.delta[11, 4000] = nan          # c of token 11 is NaN in one column
     wl.prefix[20, 7] = inf            # c of token 20 is infinite in one column
     ref = oracle.run_workload(wl, n_threads=NT)
