@@ -53,8 +53,8 @@ struct Plan {
 //    T = 256: 7.6 -> 6.4 µs), its rows in registers (up to two bank rows;
 //    7 vectors per thread, or 4 where that fits more CTAs per SM) or, for
 //    more rows or more tokens, in shared memory (7 vectors per thread, two
-//    CTAs per SM; 4 bank rows, T = 256: 10.1 -> 9.4 µs; one bank row,
-//    T = 4096: 52.8 -> 47.5 µs);
+//    CTAs per SM, one from 6 bank rows; 4 bank rows, T = 256: 10.1 -> 9.4
+//    µs; one bank row, T = 4096: 52.8 -> 47.5 µs);
 //  * with an output norm, 3..5 bank rows and at least 512 tokens: the staged
 //    form of the stream kernel (prefix and delta also in the ring) in the
 //    shape of the tuned register form, (4,4) at 5 CTAs per SM for 3 bank
@@ -63,8 +63,9 @@ struct Plan {
 //    at 5;
 //  * otherwise the stream kernel, persistent clusters with a 2-deep TMA ring,
 //    shape (CTAs per token, vectors per thread, stages):
-//      (7,4,2) with 1..5 bank rows and an output norm: one warp per CTA, so
-//              fewer warps share the reduction and exchange work of a token;
+//      (7,4,2) with 1..5 bank rows and an output norm, and 3..6 bank rows
+//              from 512 token rows: one warp per CTA, so fewer warps share
+//              the reduction and exchange work of a token;
 //      (2,8,2) with no bank rows (output norm only): 2 CTAs of 2 warps per
 //              token, so a token's short exchange spans only two CTAs, and
 //              four such CTAs fit an SM;
@@ -100,6 +101,7 @@ void auto_plan(int64_t T, int S, bool has_onorm, bool grouped, Plan* pl) {
       case 3: return many ? staged(4, 5) : row(SMEM, 7);
       case 4: return many ? staged(7, 7) : row(SMEM, 7);
       case 5: return many ? staged(4, 4) : row(SMEM, 7);
+      case 6: if (!many) return row(SMEM, 7); break;
       default: break;
     }
   } else if (!many) {
@@ -158,7 +160,11 @@ attn_res_status_t make_plan(int64_t T, int num_blocks, bool has_onorm, uint32_t 
     }
     if (pl.stages == 0) pl.stages = 2;
     if (pl.vpt == 0) {
-      const bool one_warp = pl.split == 7 && num_blocks >= 1 && num_blocks <= 5 && has_onorm;
+      // one warp per CTA: 1..5 bank rows with an output norm, and 3..6 bank
+      // rows from 512 token rows with or without it (measured 1.5-2 % faster
+      // than two warps there once the ring's start is staggered)
+      const bool one_warp = pl.split == 7 && ((num_blocks >= 1 && num_blocks <= 5 && has_onorm) ||
+                                              (num_blocks >= 3 && num_blocks <= 6 && T >= kManyTokens));
       if (!grouped && pl.split == 2)
         pl.vpt = no_bank ? 8 : 4;  // (2,8,2): measured 2-5 % faster than (2,4,2) without bank rows
       else

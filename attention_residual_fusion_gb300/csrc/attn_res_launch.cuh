@@ -232,9 +232,10 @@ cudaError_t launch_row(const Params& p, int64_t T, bool pdl, cudaStream_t stream
 }
 
 // The row kernel with its rows in shared memory: built for kRowSmemMinBlocks
-// .. kRowSmemMaxBlocks bank rows (two CTAs of up to 7 rows fit an SM).
+// .. kRowSmemMaxBlocks bank rows (two CTAs of up to 7 rows fit an SM, one
+// CTA of up to 10 rows).
 constexpr int kRowSmemMinBlocks = 1;
-constexpr int kRowSmemMaxBlocks = 5;
+constexpr int kRowSmemMaxBlocks = 8;
 
 template <int S, bool D, bool O, int VPT>
 cudaError_t launch_row_smem(const Params& p, int64_t T, bool pdl, cudaStream_t stream) {

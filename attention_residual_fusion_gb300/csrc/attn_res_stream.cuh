@@ -22,6 +22,9 @@
 //     `empty` mbarrier; thread 0 waits on it, the issuing lanes fence the
 //     generic-proxy reads against the async proxy and refill the stage with
 //     the token STAGES ahead;
+//   * the first token's rows are requested first, the other stages once they
+//     have landed (a staggered start, so the first token's work overlaps the
+//     next token's loads);
 //   * dependents of a PDL launch are released only when this CTA has run
 //     out of tokens (the grid holds every SM until then);
 //   * the token phases run software-pipelined: B(j) (softmax, mix), refill,
@@ -216,16 +219,19 @@ __device__ __forceinline__ void stream_body(const Params& p, const int64_t T) {
     }
   };
 
-  // prologue: bank rows of the first STAGES tokens before the grid-dependency
-  // wait; prefix and delta (produced upstream) after it.  Thread 0 also
-  // tracks the stages whose last issued copies it has not yet seen complete,
-  // and that issue's parity.
+  // prologue: the first token's bank rows before the grid-dependency wait;
+  // prefix and delta (produced upstream) after it.  The ring's other stages
+  // are requested only once the first token's rows have landed (phase A): a
+  // staggered start.  Requesting every stage of every CTA at once made the
+  // DRAM interleave them all, so the first token's rows landed only at the
+  // end of the whole burst and its work could not overlap the next token's
+  // loads (measured: decode T = 256 13.9 -> 12.7 µs, T = 1024 with 4 bank
+  // rows 23.4 -> 21.9 µs).  Thread 0 also tracks the stages whose last issued
+  // copies it has not yet seen complete, and that issue's parity.
   uint32_t pending = 0, pending_parity = 0;
-  if (warp == 0) {
-    for (int s = 0; s < STAGES && s < ntok; ++s) {
-      issue_bank(cid + s * ncl, s);
-      pending |= 1u << s;  // first use of every stage: parity 0 (tracked by thread 0)
-    }
+  if (warp == 0 && ntok > 0) {
+    issue_bank(cid, 0);
+    pending = 1u;  // first use of a stage: parity 0 (tracked by thread 0)
   }
   // weights: read-only, independent of the preceding kernel
   uint4 rw[VPT], qw[VPT], ow[VPT];
@@ -243,8 +249,7 @@ __device__ __forceinline__ void stream_body(const Params& p, const int64_t T) {
   grid_dep_wait();  // every thread: also orders our stores after the producer's work
   uint4 pre[VPT], del[VPT];  // prefix and delta of the next token to start
   if constexpr (STAGED) {
-    if (warp == 0)
-      for (int s = 0; s < STAGES && s < ntok; ++s) issue_current(cid + s * ncl, s);
+    if (warp == 0 && ntok > 0) issue_current(cid, 0);
   } else {
     if (ntok > 0) load_current(cid, pre, del);
   }
@@ -272,6 +277,15 @@ __device__ __forceinline__ void stream_body(const Params& p, const int64_t T) {
     wait_or_flag(smem_addr(&full_bar[s]), (uint32_t)((j / STAGES) & 1), failed, p.err,
                  kErrStageTimeout);
     if (tid == 0 && !was_failed && !failed) pending &= ~(1u << s);
+    // staggered start: token j + 1's rows go out once token j's have landed,
+    // until every stage has been used once (first use: parity 0)
+    if (warp == 0 && j + 1 < STAGES && j + 1 < ntok &&
+        !__any_sync(0xffffffffu, failed)) {
+      const int s1 = (int)(j + 1);
+      issue_bank(cid + (j + 1) * ncl, s1);
+      issue_current(cid + (j + 1) * ncl, s1);
+      pending |= 1u << s1;
+    }
     const uint4* stage = stage_of(j);
     if constexpr (STAGED) {
 #pragma unroll

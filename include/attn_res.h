@@ -90,7 +90,7 @@ typedef enum {
  *              ATTN_RES_KERNEL_ROW -- one CTA per token row holding the whole
  *              row in registers, no cluster (up to 2 bank rows);
  *              ATTN_RES_KERNEL_ROW_SMEM -- the same with the rows in shared
- *              memory, brought in by bulk copies (1..5 bank rows).
+ *              memory, brought in by bulk copies (1..8 bank rows).
  *   SPLIT(k):  CTAs (one thread-block cluster) a token row is split over;
  *              split kernel 4, 7, 8, 14 or 16; stream kernel see below; the
  *              row kernels 1.
@@ -102,8 +102,9 @@ typedef enum {
  * (4,2,2) (4,2,3) (2,4,2) (14,2,2) (2,8,2).  Unset fields default to:
  * split 2 with no bank rows (4 if VPT 2 is given, 7 for VPT 1), else 7;
  * stages 2; VPT 8 with split 2 and no bank rows, 4 with split 2 and bank
- * rows or with split 7, 1..5 bank rows and an output norm, else 2 -- so
- * (7,4,2), (2,8,2) with no bank rows, and (7,2,2) otherwise.
+ * rows, or with split 7 and 1..5 bank rows and an output norm or 3..6 bank
+ * rows from 512 token rows, else 2 -- so (7,4,2) there, (2,8,2) with no
+ * bank rows, and (7,2,2) otherwise.
  * Staged shapes (split, vpt, CTAs per SM): (4,4,5) (7,4,7) (4,4,4); the
  * ring holds as many stages of the S + 1 (+1 with delta) row slices as fit,
  * and a shape whose ring cannot hold two is ATTN_RES_EINVAL for that S.
@@ -116,7 +117,8 @@ typedef enum {
  *   the row kernel below 512 rows and the shared-memory row kernel from
  *   512; 2, the row kernel below 4096 rows and the shared-memory one from
  *   4096; 3..5, the shared-memory row kernel below 512 rows and the staged
- *   form from 512; 6..8, the stream kernel;
+ *   form from 512; 6, the shared-memory row kernel below 512 rows and the
+ *   stream kernel from 512; 7..8, the stream kernel;
  *   without an output norm, below 512 rows: no bank row, the split kernel;
  *   1..2, the row kernel; 3, the staged form; 4..5, the shared-memory row
  *   kernel; 6..8, the stream kernel; from 512 rows: 0..1 bank rows, the row

@@ -52,7 +52,9 @@ def test_launch_shape(lib):
     assert ls(8192, 4, True, has_delta=False)["stages"] == 3
     assert ls(256, 4, True) == dict(kernel="row_smem", split=1, stages=0, threads=128, ctas=256, cluster=1)
     assert ls(256, 4, True, ar.FLAG_KERNEL(2)) == dict(kernel="stream", split=7, stages=2, threads=32, ctas=0, cluster=7)
-    assert ls(8192, 4, False) == dict(kernel="stream", split=7, stages=2, threads=64, ctas=0, cluster=7)
+    assert ls(8192, 4, False) == dict(kernel="stream", split=7, stages=2, threads=32, ctas=0, cluster=7)
+    assert ls(256, 4, False)["kernel"] == "row_smem" and ls(256, 7, False)["threads"] == 64
+    assert ls(256, 6, True)["kernel"] == "row_smem" and ls(1024, 6, True)["threads"] == 32
     assert ls(2048, 3, True)["kernel"] == "staged" and ls(2048, 5, True)["kernel"] == "staged"
     assert ls(256, 3, False) == dict(kernel="staged", split=4, stages=2, threads=64, ctas=0, cluster=4)
     assert ls(2048, 6, True)["kernel"] == "stream"
@@ -87,7 +89,7 @@ def test_launch_shape(lib):
                 (1, 1, 0, ar.FLAG_KERNEL(7)), (1, 1, 0, ar.FLAG_KERNEL(2) | ar.FLAG_SPLIT(16)),
                 (1, 3, 0, ar.FLAG_KERNEL(5)), (1, 0, 0, ar.FLAG_KERNEL(5) | ar.FLAG_VPT(2)),
                 (1, 0, 0, ar.FLAG_KERNEL(5) | ar.FLAG_SPLIT(2)),
-                (1, 0, 0, ar.FLAG_KERNEL(6)), (1, 6, 0, ar.FLAG_KERNEL(6)),
+                (1, 0, 0, ar.FLAG_KERNEL(6)),
                 (1, 3, 0, ar.FLAG_KERNEL(6) | ar.FLAG_VPT(1)),
                 (1, 8, 0, ar.FLAG_KERNEL(4)),
                 (1, 2, 0, ar.FLAG_KERNEL(4) | ar.FLAG_SPLIT(7) | ar.FLAG_VPT(2) | ar.FLAG_STAGES(2)),

@@ -266,14 +266,14 @@ def test_row_kernel(S, vpt, d, o):
     full_check(wl, tag=f"row_S{S}_v{vpt}_d{int(d)}_o{int(o)}_w{w}", kernel=ar.KERNEL_ROW, vpt=vpt)
 
 
-ROW_SMEM_CASES = [(S, v, d, o) for S in range(1, 6) for v in ROW_VPTS for d in (False, True)
+ROW_SMEM_CASES = [(S, v, d, o) for S in range(1, 9) for v in ROW_VPTS for d in (False, True)
                   for o in (False, True)]
 
 
 @pytest.mark.parametrize("S,vpt,d,o", ROW_SMEM_CASES,
                          ids=[f"S{S}_v{v}_d{int(d)}_o{int(o)}" for S, v, d, o in ROW_SMEM_CASES])
 def test_row_smem_kernel(S, vpt, d, o):
-    """The row kernel with its rows in shared memory: 1..5 bank rows x
+    """The row kernel with its rows in shared memory: 1..8 bank rows x
     vectors per thread x delta x output norm, write-back slot and padded
     bank slots varying by case."""
     i = ROW_SMEM_CASES.index((S, vpt, d, o))
@@ -452,9 +452,9 @@ GROUPED = [(B, T, S, w, k) for B in (2, 3, 8) for (T, S, w) in ((5, 4, -1), (37,
                                                                  (300, 0, 2), (37, 1, 5))
            for k in (ar.KERNEL_SPLIT, ar.KERNEL_STREAM, ar.KERNEL_GENERIC, ar.KERNEL_ROW,
                      ar.KERNEL_ROW_SMEM)
-           # the row kernels are built for up to two (registers) and 1..5 bank
+           # the row kernels are built for up to two (registers) and 1..8 bank
            # rows (shared memory)
-           if (k != ar.KERNEL_ROW or S <= 2) and (k != ar.KERNEL_ROW_SMEM or 1 <= S <= 5)]
+           if (k != ar.KERNEL_ROW or S <= 2) and (k != ar.KERNEL_ROW_SMEM or S >= 1)]
 
 
 @pytest.mark.parametrize("B,T,S,w,kernel", GROUPED,
