@@ -513,11 +513,14 @@ __global__ void __launch_bounds__(TpRingCfg<S, HAS_DELTA, PHASE, HAS_ONORM, GRAM
   };
 
   // thread 0 tracks the stages whose last issued copies it has not yet seen
-  // complete, and that issue's parity
+  // complete, and that issue's parity.  Staggered start: only the first
+  // token's rows now; the other stages once they have landed (in the loop),
+  // so the first token's work overlaps the next token's loads instead of
+  // every CTA's whole ring arriving at once at the end of one burst.
   uint32_t pending = 0, pending_parity = 0;
-  if (warp == 0) {
-    for (int j = 0; j < stages && j < ntok; ++j) issue(j, j);
-    if (tid == 0) pending = (1u << (ntok < stages ? (int)ntok : stages)) - 1u;
+  if (warp == 0 && ntok > 0) {
+    issue(0, 0);
+    pending = 1u;
   }
   if (NS > 0) {
     float first[2] = {0.f, 0.f};
@@ -575,6 +578,11 @@ __global__ void __launch_bounds__(TpRingCfg<S, HAS_DELTA, PHASE, HAS_ONORM, GRAM
     const bool was_failed = failed;
     wait_or_flag(smem_addr(&full_bar[s]), parity, failed, p.err, kErrStageTimeout);
     if (tid == 0 && !was_failed && !failed) pending &= ~(1u << s);
+    // staggered start: token j + 1 into its first (unused) stage
+    if (warp == 0 && j + 1 < stages && j + 1 < ntok && !__any_sync(0xffffffffu, failed)) {
+      issue(j + 1, (int)(j + 1));
+      pending |= 1u << (int)(j + 1);
+    }
     uint4* const st = ring + (int64_t)s * ROWS * pv;
     auto src = [&](int i, int64_t v) { return st[i * pv + v]; };
     auto cur = [&](int64_t v) {

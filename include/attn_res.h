@@ -284,6 +284,11 @@ attn_res_status_t attn_res_h(int64_t H, attn_res_bf16_t* prefix,
  * call (which rejects the flag).  Exact in real arithmetic; in fp32 the
  * output norm loses relative accuracy where the weighted rows cancel
  * (|acc| << sum_i w_i |x_i|), so the default is the two-exchange form.
+ * The ring form computes the Gram products on warp-level tensor-core tiles
+ * (mma.sync m16n8k16, bf16 in, fp32 accumulate; q split exactly into two
+ * bf16 rows): the one dense contraction in this library, confined to this
+ * opt-in form -- the mixture itself, like the pages' kernels, uses no tensor
+ * cores (a bandwidth-bound mix of a few rows per token).
  */
 
 /* Floats per token row of `sums`: 2N, plus N(N-1)/2 with gram != 0
