@@ -123,9 +123,9 @@ __global__ void __launch_bounds__(SplitCfg<S, HAS_DELTA, HAS_ONORM, K>::THREADS)
       st_row(const_cast<uint16_t*>(bank_of(p, t)) + (int64_t)p.write_idx * p.blocks_slot + col,
              c[0]);
   }
-  // after a time-out anywhere in the CTA: no peer's sums may still land here
-  // once it exits
-  if (COMM && __syncthreads_or(failed) && tid == 0) mailbox_drain<Tok>(mb, 0, HAS_ONORM);
+  // a thread whose wait timed out does not leave before the peers' sums it
+  // gave up on have landed (bounded): the CTA stays resident until then
+  if (COMM && failed) mailbox_drain<Tok>(mb, 0, HAS_ONORM);
 }
 
 }  // namespace attn_res_dev

@@ -371,14 +371,17 @@ __device__ __forceinline__ void stream_body(const Params& p, const int64_t T) {
   // of taking SM slots from clusters still streaming.
   grid_dep_launch_dependents();
 
-  // After a time-out anywhere in the CTA, do not leave with copies or a
-  // peer's partial sums still landing in shared memory.
-  if (__syncthreads_or(failed) && tid == 0) {
+  // After a time-out, do not leave with copies or a peer's partial sums still
+  // landing in shared memory: thread 0 (the only one that issues copies, and
+  // only while it has not failed) waits, bounded, for the copies it has not
+  // seen complete; any thread whose wait timed out waits for the last armed
+  // mailbox phases.  The CTA stays resident until its threads are done.
+  if (tid == 0 && failed) {
     for (int s = 0; s < STAGES; ++s)
       if (pending & (1u << s))
         (void)mbar_wait_bounded(smem_addr(&full_bar[s]), (pending_parity >> s) & 1u);
-    if (COMM) mailbox_drain<Tok>(mb, ntok - 1, HAS_ONORM);
   }
+  if (COMM && failed) mailbox_drain<Tok>(mb, ntok - 1, HAS_ONORM);
 }
 
 template <int S, bool HAS_DELTA, bool HAS_ONORM, int K, int VPT, int STAGES, bool GROUPED,

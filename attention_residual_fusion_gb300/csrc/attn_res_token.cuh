@@ -97,10 +97,11 @@ __device__ __forceinline__ void mailbox_expect(typename Cfg::Box& mb, int b, boo
   if (has_onorm) mbar_arrive_expect_tx(smem_addr(&mb.bar_sq[b]), senders * 4u);
 }
 
-// Time-out path only (thread 0, at exit): wait, bounded, for the last phase
-// armed on each mailbox buffer -- token `last` and the one before it -- so
-// that no peer's partial sums still land in this CTA's shared memory after it
-// exits.  A phase that already completed returns at once.
+// Time-out path only (a thread whose wait gave up, at exit): wait, bounded,
+// for the last phase armed on each mailbox buffer -- token `last` and the one
+// before it -- so that no peer's partial sums still land in this CTA's shared
+// memory after it exits.  A phase that already completed returns at once;
+// several threads may wait on one phase.
 template <class Cfg>
 __device__ __forceinline__ void mailbox_drain(typename Cfg::Box& mb, int64_t last, bool has_onorm) {
   for (int64_t j = last; j >= 0 && j >= last - 1; --j) {
