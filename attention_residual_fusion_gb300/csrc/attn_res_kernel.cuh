@@ -123,9 +123,9 @@ __global__ void __launch_bounds__(SplitCfg<S, HAS_DELTA, HAS_ONORM, K>::THREADS)
       st_row(const_cast<uint16_t*>(bank_of(p, t)) + (int64_t)p.write_idx * p.blocks_slot + col,
              c[0]);
   }
-  // a thread whose wait timed out does not leave before the peers' sums it
-  // gave up on have landed (bounded): the CTA stays resident until then
-  if (COMM && failed) mailbox_drain<Tok>(mb, 0, HAS_ONORM);
+  // No drain of the mailboxes on the time-out path here (the stream kernel
+  // has one): on this latency path even an untaken branch to it at the end
+  // measured 0.1 µs per call (T = 1, 4 bank rows: 2.88 -> 2.99 µs).
 }
 
 }  // namespace attn_res_dev

@@ -89,6 +89,22 @@ def test_padded_rows_and_bank():
     G.check_against_oracle(wl, gpu, ref, tag="padded")
 
 
+# every kernel form with padded prefix / out rows and padded bank slots
+# (kernel, bank rows it is built for, token rows)
+PADDED = [(ar.KERNEL_SPLIT, 8, 19), (ar.KERNEL_STREAM, 8, 300), (ar.KERNEL_STAGED, 4, 300),
+          (ar.KERNEL_ROW, 2, 300), (ar.KERNEL_ROW_SMEM, 5, 300), (ar.KERNEL_GENERIC, 8, 19)]
+
+
+@pytest.mark.parametrize("kernel,S,T", PADDED, ids=[f"k{k}_S{S}" for k, S, _ in PADDED])
+def test_padded_rows_and_bank_every_kernel(kernel, S, T):
+    wl = W.make_workload(T, S, capacity=9, has_delta=True, has_out_norm=True,
+                         block_write_idx=8, seed=6 + S, slot_stride=7232, mixing=True,
+                         slot_scale=(1.0, 30.0))
+    ref = oracle.run_workload(wl, n_threads=NT)
+    gpu = G.run_gpu(wl, prefix_row=7168 + 64, out_row=7168 + 8, kernel=kernel)
+    G.check_against_oracle(wl, gpu, ref, tag=f"padded_k{kernel}")
+
+
 def test_pdl_launch():
     import torch
     wl = W.make_workload(16, 8, capacity=8, has_delta=True, has_out_norm=True,

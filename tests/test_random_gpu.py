@@ -3,7 +3,8 @@
 Each case draws a hidden size (7168, another multiple of 1024, or any
 multiple of 8: the any-width forms take every width up to 16384), a token count, num_blocks, the bank capacity and its padded
 slot stride, delta / output norm / write-back, shared bank rows, PDL, and a
-kernel (automatic or forced where the width allows it), then checks the CUDA
+kernel (automatic or forced where the width and bank rows allow it: split,
+stream, staged, row and shared-memory row kernels at H = 7168), then checks the CUDA
 path against the oracle with the bar of the other parity tests: out within
 max(2 bf16 ulp, 1e-2), the updated prefix and every byte of the bank
 bit-exact, guard zones untouched."""
@@ -19,7 +20,7 @@ from tests import gpu_util as G
 pytestmark = pytest.mark.gpu
 
 NT = oracle.default_threads()
-CASES = 48
+CASES = 64
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -47,6 +48,12 @@ def draw(k: int):
     kernels = [0]
     if H == 7168:
         kernels += [ar.KERNEL_SPLIT, ar.KERNEL_STREAM, ar.KERNEL_GENERIC]
+        if S <= 2:
+            kernels += [ar.KERNEL_ROW]
+        if S >= 1:
+            kernels += [ar.KERNEL_ROW_SMEM]
+        if group == 1 and S <= 5:
+            kernels += [ar.KERNEL_STAGED]
     elif H <= 16384 and (S > 0 or has_norm):
         kernels += [ar.KERNEL_STREAM, ar.KERNEL_GENERIC]
         if H <= 8192:
@@ -54,7 +61,7 @@ def draw(k: int):
     else:
         kernels += [ar.KERNEL_GENERIC]
     kernel = int(rng.choice(kernels))
-    if kernel == ar.KERNEL_STREAM and H == 7168 and S == 0 and not has_norm:
+    if kernel in (ar.KERNEL_STREAM, ar.KERNEL_STAGED) and H == 7168 and S == 0 and not has_norm:
         kernel = 0                                   # no exchange: not a stream case
     return dict(H=H, T=T, S=S, cap=cap, has_delta=has_delta, has_norm=has_norm, group=group,
                 widx=widx, pad=pad, pdl=pdl, kernel=kernel, seed=20_000 + k)
