@@ -558,6 +558,14 @@ __global__ void __launch_bounds__(TpRingCfg<S, HAS_DELTA, PHASE, HAS_ONORM, GRAM
   }
   if (NS > 0 || MMA) __syncthreads();
 
+  // plain sums with at most one vector per thread (the shard fits the CTA):
+  // the thread's query vector once, not per token
+  const bool one_vec = nv <= nthr;
+  f32x2 q_own[4] = {};
+  if constexpr (PHASE == 0 && !GRAM) {
+    if (one_vec && tid < nv) tp_query(p, tid * kVec, q_own);
+  }
+
   bool failed = false;
   int s = 0;            // stage of local token j: j % stages
   uint32_t parity = 0;  // its phase parity: (j / stages) & 1
@@ -595,7 +603,12 @@ __global__ void __launch_bounds__(TpRingCfg<S, HAS_DELTA, PHASE, HAS_ONORM, GRAM
       tp_clear<S, false>(ss, dt, part);
       for (int64_t v = tid; v < nv; v += nthr) {
         f32x2 q[4];
-        tp_query(p, v * kVec, q);
+        if (one_vec) {
+#pragma unroll
+          for (int k = 0; k < 4; ++k) q[k] = q_own[k];
+        } else {
+          tp_query(p, v * kVec, q);
+        }
         uint4 x[N];
         tp_gather<S>([&](int i) { return src(i, v); }, cur(v), x);
         tp_accumulate<S, false>(x, q, ss, dt, part);
@@ -603,10 +616,17 @@ __global__ void __launch_bounds__(TpRingCfg<S, HAS_DELTA, PHASE, HAS_ONORM, GRAM
       tp_fold<S, false>(ss, dt, part);
       cta_sum_store<NT>(part, scratch[b], [&](int r, float v) { a.sums[t * a.sums_row + r] = v; });
     } else if constexpr (MMA) {
-      // c into the stage's prefix row, so that rows 0..S are the sources
+      const int k16 = (int)((nv + 1) >> 1);  // 16-column steps (the last may be half)
+      // c into the stage's prefix row, so that rows 0..S are the sources --
+      // each warp for the two vectors of each 16-column step it multiplies
+      // below (steps warp, warp + nw, ...), so a warp barrier suffices
       if constexpr (HAS_DELTA) {
-        for (int64_t v = tid; v < nv; v += nthr) st[S * pv + v] = cur(v);
-        __syncthreads();
+        const int nsteps = warp < k16 ? (k16 - 1 - warp) / nw + 1 : 0;
+        for (int e = lane; e < 2 * nsteps; e += 32) {
+          const int64_t v = 2 * (int64_t)(warp + (e >> 1) * nw) + (e & 1);
+          if (v < nv) st[S * pv + v] = cur(v);
+        }
+        __syncwarp();
       }
       const uint32_t sb = ring_addr + (uint32_t)s * stage_bytes;
       const uint32_t arow = sb + (uint32_t)am * pitch;
@@ -615,7 +635,6 @@ __global__ void __launch_bounds__(TpRingCfg<S, HAS_DELTA, PHASE, HAS_ONORM, GRAM
       // two accumulator sets (even and odd steps of this warp) halve the
       // chain of dependent mma
       float d[2][2][4] = {};
-      const int k16 = (int)((nv + 1) >> 1);  // 16-column steps (the last may be half)
       auto step = [&](int ks, float(&e)[2][4]) {
         const uint32_t ca = (uint32_t)ks * 16u + ak, cb = (uint32_t)ks * 16u + bk;
         uint32_t av[4], bv[4];
