@@ -116,8 +116,8 @@ def kernel_label(wl, shape) -> str:
         v = -(-vpc // shape["threads"])  # vectors per thread
         return (f"attn_res_stream_kernel<{wl.num_blocks},{d},{o},{shape['split']},{v},"
                 f"{shape['stages']},{int(wl.group > 1)},{int(shape['kernel'] == 'staged')}>")
-    if shape["kernel"] == "row":
-        return f"attn_res_row_kernel<{wl.num_blocks},{d},{o},{896 // shape['threads']}>"
+    if shape["kernel"] in ("row", "row_smem"):
+        return f"attn_res_{shape['kernel']}_kernel<{wl.num_blocks},{d},{o},{896 // shape['threads']}>"
     if shape["kernel"] == "split":
         return f"attn_res_split_kernel<{wl.num_blocks},{d},{o},{shape['split']}>"
     return f"attn_res_{shape['kernel']}_kernel<{wl.num_blocks},{d},{o}>"
