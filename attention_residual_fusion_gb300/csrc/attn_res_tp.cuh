@@ -400,9 +400,11 @@ __global__ void __launch_bounds__(kTpMaxThreads) attn_res_tp_finish_kernel(const
 // taken from them while the token's rows are still arriving.  Waits are
 // bounded as in the stream kernel.  The arithmetic per element is that of the
 // kernels above, except that the Gram sums (45 dot products of 9 rows per
-// token at S = 8: a small dense contraction) run on mma.sync tiles: A and B
-// are the stage's rows (plus the query split into two exact bf16 rows), 16
-// columns per step, the warps' 16 x 16 tiles summed in warp order.  (tcgen05
+// token at S = 8: a small dense contraction) run on mma.sync tiles: per step
+// of 16 columns one 16 x 16 tile X holds the stage's rows (plus the query
+// split into two exact bf16 rows), read once with ldmatrix, and X X^T takes
+// two m16n8k16 mma whose B operands are A's own registers; the warps'
+// 16 x 16 tiles are summed in warp order.  (tcgen05
 // wants tiles of at least 64 rows in its core-matrix layout; a token has 9
 // rows, stored row-major.)
 //
@@ -527,16 +529,18 @@ __global__ void __launch_bounds__(TpRingCfg<S, HAS_DELTA, PHASE, HAS_ONORM, GRAM
     if (ntok > 0) load_reduced(0, first);
     store_reduced(sv[0], first);
   }
-  // MMA: lane l addresses row l % 8 of 8x8 matrix l / 8 of A (rows m: the
-  // sources, then zeros) and of B (rows n: the sources, q_hi, q_lo, zeros),
-  // both stored [row][column]
-  int am = 0, ak = 0, bn = 0, bk = 0;
+  // MMA: lane l addresses row l % 8 of 8x8 matrix l / 8 of the 16 x 16 tile
+  // X of a step (rows: the sources, q_hi, q_lo, zeros; stored
+  // [row][column]): matrices 0..3 = (rows 0-7 | 8-15) x (columns 0-7 | 8-15)
+  // in the order of the A operand's registers.  The products wanted are
+  // X X^T, and the B operand of X^T (16 x 8, column-major) for rows 0-7 of X
+  // is A's registers 0 and 2, for rows 8-15 registers 1 and 3: one ldmatrix
+  // per step serves both operands.
+  int am = 0, ak = 0;
   if constexpr (MMA) {
     const int mj = lane >> 3, mr = lane & 7;
     am = (mj & 1) * 8 + mr;
     ak = (mj >> 1) * 8;
-    bn = (mj >> 1) * 8 + mr;
-    bk = (mj & 1) * 8;
     for (int64_t v = tid; v < nv; v += nthr) {
       f32x2 q[4];
       tp_query(p, v * kVec, q);
@@ -629,26 +633,33 @@ __global__ void __launch_bounds__(TpRingCfg<S, HAS_DELTA, PHASE, HAS_ONORM, GRAM
         __syncwarp();
       }
       const uint32_t sb = ring_addr + (uint32_t)s * stage_bytes;
-      const uint32_t arow = sb + (uint32_t)am * pitch;
-      const uint32_t brow = bn < N ? sb + (uint32_t)bn * pitch : bn == N ? qhi_addr : qlo_addr;
-      const bool bvalid = bn < N + 2;
+      const uint32_t arow = am < N ? sb + (uint32_t)am * pitch : am == N ? qhi_addr : qlo_addr;
+      const bool avalid = am < N + 2;
       // two accumulator sets (even and odd steps of this warp) halve the
-      // chain of dependent mma
+      // chain of dependent mma; the tiles of the next two steps are read
+      // while the current two multiply (steps past the row read the zero
+      // bytes and add nothing)
       float d[2][2][4] = {};
-      auto step = [&](int ks, float(&e)[2][4]) {
-        const uint32_t ca = (uint32_t)ks * 16u + ak, cb = (uint32_t)ks * 16u + bk;
-        uint32_t av[4], bv[4];
-        ldsm_x4(am < N && ca < a.Hs ? arow + ca * 2u : zero_addr, av);
-        ldsm_x4(bvalid && cb < a.Hs ? brow + cb * 2u : zero_addr, bv);
-        mma_bf16_16x8x16(e[0], av, bv[0], bv[1]);
-        mma_bf16_16x8x16(e[1], av, bv[2], bv[3]);
+      auto load = [&](int ks, uint32_t(&av)[4]) {
+        const uint32_t ca = (uint32_t)ks * 16u + ak;
+        ldsm_x4(avalid && ks < k16 && ca < a.Hs ? arow + ca * 2u : zero_addr, av);
       };
-      int ks = warp;
-      for (; ks + nw < k16; ks += 2 * nw) {
-        step(ks, d[0]);
-        step(ks + nw, d[1]);
+      auto mul = [&](const uint32_t(&av)[4], float(&e)[2][4]) {
+        mma_bf16_16x8x16(e[0], av, av[0], av[2]);
+        mma_bf16_16x8x16(e[1], av, av[1], av[3]);
+      };
+      uint32_t x0[4], x1[4];
+      load(warp, x0);
+      load(warp + nw, x1);
+      for (int ks = warp; ks < k16; ks += 2 * nw) {
+        uint32_t y0[4], y1[4];
+        load(ks + 2 * nw, y0);
+        load(ks + 3 * nw, y1);
+        mul(x0, d[0]);
+        mul(x1, d[1]);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) x0[e] = y0[e], x1[e] = y1[e];
       }
-      if (ks < k16) step(ks, d[0]);
       float d0[4], d1[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
