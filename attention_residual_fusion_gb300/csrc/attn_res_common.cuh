@@ -106,6 +106,14 @@ __device__ __forceinline__ uint32_t cluster_nctarank() {
 __device__ __forceinline__ void cluster_arrive_release() {
   asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
 }
+// Arrival without release semantics: pairs with fence_mbar_init() in the
+// thread that initialised the barriers peers will use (the release of those
+// initialisations at cluster scope, per the PTX ISA's fence.mbarrier_init),
+// so the arrival itself orders nothing.  The release form measured ~0.43 µs
+// between a CTA's start and its first bulk copy.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
 __device__ __forceinline__ void cluster_wait_acquire() {
   asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }

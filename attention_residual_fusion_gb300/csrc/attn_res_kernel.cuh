@@ -72,10 +72,10 @@ __global__ void __launch_bounds__(SplitCfg<S, HAS_DELTA, HAS_ONORM, K>::THREADS)
       fence_mbar_init();
       mailbox_expect<Tok>(mb, 0, HAS_ONORM, sp);
     }
-    // Announce this CTA (and its initialised mailboxes) to the cluster; the
-    // matching wait, just before the first remote store, guarantees every
-    // peer is running and ready to receive.
-    cluster_arrive_release();
+    // Announce this CTA (its mailboxes initialised and released by the fence
+    // above) to the cluster; the matching wait, just before the first remote
+    // store, guarantees every peer is running and ready to receive.
+    cluster_arrive_relaxed();
   }
 
   // 1. bank rows: independent of the preceding kernel

@@ -176,12 +176,6 @@ __device__ __forceinline__ void stream_body(const Params& p, const int64_t T) {
     for (int e = tid; e < STAGES * C::RING_ROWS * tail; e += THREADS)
       ring[(e / tail) * VPC + (int)(slice_bytes / 16) + e % tail] = make_uint4(0, 0, 0, 0);
   }
-  if (COMM) {
-    cluster_arrive_release();  // matched by the wait before the first remote store
-  } else {
-    __syncthreads();
-  }
-
   // producer side (every lane of warp 0): the bank rows of one token into one
   // stage -- lane 0 arms the stage's barrier with the byte count of the whole
   // stage, then lane i < S issues the copy of bank row i, so the S copies go
@@ -228,10 +222,25 @@ __device__ __forceinline__ void stream_body(const Params& p, const int64_t T) {
   // loads (measured: decode T = 256 13.9 -> 12.7 µs, T = 1024 with 4 bank
   // rows 23.4 -> 21.9 µs).  Thread 0 also tracks the stages whose last issued
   // copies it has not yet seen complete, and that issue's parity.
+  // The first copies go out before the cluster arrival: thread 0 initialised
+  // the stage barrier (released by its fence above) and arms it, and the
+  // warp barrier in issue_bank orders that before the other lanes' copies.
   uint32_t pending = 0, pending_parity = 0;
   if (warp == 0 && ntok > 0) {
     issue_bank(cid, 0);
     pending = 1u;  // first use of a stage: parity 0 (tracked by thread 0)
+  }
+  if (COMM) {
+    // matched by the wait before the first remote store; the mailbox
+    // barriers were released by thread 0's fence, the ragged zero fill needs
+    // the release of the arrival itself
+    if constexpr (RAGGED) {
+      cluster_arrive_release();
+    } else {
+      cluster_arrive_relaxed();
+    }
+  } else {
+    __syncthreads();
   }
   // weights: read-only, independent of the preceding kernel
   uint4 rw[VPT], qw[VPT], ow[VPT];
