@@ -22,7 +22,8 @@
 //     `empty` mbarrier; thread 0 waits on it, the issuing lanes fence the
 //     generic-proxy reads against the async proxy and refill the stage with
 //     the token STAGES ahead;
-//   * the first token's rows are requested first, the other stages once they
+//   * the first token's rows are requested first -- right after the barrier
+//     set-up, before the cluster arrival -- and the other stages once they
 //     have landed (a staggered start, so the first token's work overlaps the
 //     next token's loads);
 //   * dependents of a PDL launch are released only when this CTA has run
