@@ -20,7 +20,7 @@ from tests import gpu_util as G
 pytestmark = pytest.mark.gpu
 
 NT = oracle.default_threads()
-CASES = 64
+CASES = 160
 
 
 @pytest.fixture(scope="module", autouse=True)
