@@ -16,7 +16,11 @@ than L2, so no flush is needed between steps.
   roofline   algorithmic bytes per launch / mean launch time vs the measured
              HBM copy bandwidth
   latency_us T=1 latency (single-token and 8-block cases): per call with an
-             L2 flush in between, and back-to-back in a CUDA graph
+             L2 flush in between (and the floor that timing has: a
+             one-element add measured the same way), back-to-back in a CUDA
+             graph on one input set, and back-to-back with every call's
+             rows in a different slot of a pool larger than 3x L2 (rows
+             from DRAM)
   pdl_chain  graph-replayed chains of calls with and without programmatic
              dependent launch (T=1 and T=1024)
   prefill_cells  T=1024/2048 prefill cells: µs per call from CUDA-graph
@@ -561,10 +565,30 @@ def pdl_chain(ar, torch, dev, stream):
 
 def latency_t1(ar, torch, dev, stream, reps=200):
     """T=1 latency: per call with L2 flushed between calls (events around each
-    call), and back-to-back inside a captured CUDA graph."""
+    call); back-to-back inside a captured CUDA graph on one input set (warm
+    L2); and back-to-back in a graph whose calls each take their rows from a
+    different slot of a pool larger than 3x L2 (each call's rows come from
+    DRAM).  `flush_floor_us` is a one-element add timed like the flushed
+    calls: the floor that timing puts under any kernel that follows the
+    flush (an add, not a fill: a kernel other than the flush's own measured
+    ~2 µs more than a second fill)."""
     from attention_residual_fusion_gb300 import workloads as W
     res = {}
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    one = torch.zeros(1, device=dev)
+    floor = []
+    for _ in range(reps):
+        with torch.cuda.stream(stream):
+            flush.fill_(1.0)
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            one.add_(1.0)
+            b.record(stream)
+        b.synchronize()
+        floor.append(a.elapsed_time(b) * 1e3)
+    res["flush_floor_us"] = round(statistics.median(floor), 3)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     for name, wl in (("single_token_T1_S4", W.single_token()),
                      ("T1_S8_delta_norm", W.variant_cell(1, 8, True, True, -1))):
         t = device_tensors(wl, torch, dev)
@@ -586,11 +610,33 @@ def latency_t1(ar, torch, dev, stream, reps=200):
         with torch.cuda.graph(g, stream=stream):
             for _ in range(n):
                 call(ar, wl, t, stream)
+        graph_us = replay_us(g, torch, stream, n)
+        del g
+        # a pool of P single-token slots (bank rows, prefix, delta, out), each
+        # call of the graph on the next slot
+        per_call = wl.algorithmic_bytes()
+        P = int(-(-3 * l2 // per_call))
+        pool = dict(prefix=t["prefix"].repeat(P, 1),
+                    delta=None if t["delta"] is None else t["delta"].repeat(P, 1),
+                    bank=t["bank"].repeat(P, 1, 1),
+                    out=torch.empty((P, wl.H), dtype=torch.bfloat16, device=dev))
+        slot = lambda i: dict(t, prefix=pool["prefix"][i:i + 1], bank=pool["bank"][i:i + 1],
+                              delta=None if pool["delta"] is None else pool["delta"][i:i + 1],
+                              out=pool["out"][i:i + 1])
+        for i in range(P):
+            call(ar, wl, slot(i), stream)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(P):
+                call(ar, wl, slot(i), stream)
+        cold_us = replay_us(g, torch, stream, P)
         res[name] = {"flushed_p50": round(statistics.median(times), 3),
                      "flushed_p20": round(float(np.percentile(times, 20)), 3),
                      "flushed_p80": round(float(np.percentile(times, 80)), 3),
-                     "graph_per_call": round(replay_us(g, torch, stream, n), 3)}
-        del t, g
+                     "graph_per_call": round(graph_us, 3),
+                     "graph_dram_per_call": round(cold_us, 3), "graph_dram_slots": P}
+        del t, g, pool
     del flush
     return res
 
@@ -814,8 +860,10 @@ def summary(line: dict, parity) -> dict:
            "headline_frac": line["roofline"]["frac"]}
     lat = line.get("latency_us")
     if lat:
-        out["t1_us"] = {k: {"flushed_p50": v["flushed_p50"], "graph": v["graph_per_call"]}
-                        for k, v in lat.items()}
+        out["t1_us"] = {k: {"flushed_p50": v["flushed_p50"], "graph": v["graph_per_call"],
+                            "graph_dram": v["graph_dram_per_call"]}
+                        for k, v in lat.items() if isinstance(v, dict)}
+        out["t1_us"]["flush_floor_us"] = lat.get("flush_floor_us")
     cells = line.get("prefill_cells")
     if cells:
         worst = min(cells, key=lambda c: c["frac"])
